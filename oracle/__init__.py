@@ -1,0 +1,14 @@
+"""fp64 CPU oracle for the attention forward pass.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import anything under
+``oracle/``. The product (the CUDA library and its Python binding) never
+does, and shares no code with it.
+
+Contents:
+  attn        -- ctypes loader of the C reference (exact definition, fp64).
+  tiled_model -- fp64 model of the tile-by-tile online softmax with the
+                 conditional (lazy) rescale, in the pages' order.
+  exp2_emu    -- model of the software 2^x (Cody-Waite range reduction +
+                 Horner polynomial) with its own minimax fit.
+"""
