@@ -1,0 +1,169 @@
+"""GB300 (sm_103a) fused attention forward: Python binding of ``libfa4.so``.
+
+Every step of the forward pass runs in the library's CUDA kernels; this
+module only checks tensor metadata, allocates outputs with torch and
+passes pointers to the C ABI declared in ``include/fa4.h``. There is no
+CPU or PyTorch fallback: if the library is missing or the device is not an
+sm_103 GPU the calls raise.
+
+    o, lse = fwd(q, k, v, causal=True)        # q [B,Sq,Hq,d], k/v [B,Sk,Hkv,d] BF16
+
+The operation is the attention forward of "FlashAttention-4: Algorithm and
+Kernel Pipelining Co-Design for Asymmetric Hardware Scaling" (Method,
+§3.1): O = softmax(scale * Q K^T [causal mask]) V and the natural-log
+LSE per row.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["fwd", "fwd_into", "exp2_eval", "device_status", "status_string", "version",
+           "lib_path", "load_library", "Fa4Error", "FA4_OK", "FA4_ERR_INVALID_ARG",
+           "FA4_ERR_UNSUPPORTED", "FA4_ERR_MISALIGNED", "FA4_ERR_CUDA", "FA4_ERR_TIMEOUT"]
+
+FA4_OK = 0
+FA4_ERR_INVALID_ARG = 1
+FA4_ERR_UNSUPPORTED = 2
+FA4_ERR_MISALIGNED = 3
+FA4_ERR_CUDA = 4
+FA4_ERR_TIMEOUT = 5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libfa4.so")
+_lib = None
+
+
+class Fa4Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code) if _lib else code}")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("tau", ctypes.c_float), ("exp2_emulation", ctypes.c_int),
+                ("rescale_stats", ctypes.c_void_p)]
+
+
+def load_library():
+    """Load ``libfa4.so`` (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(lib_path):
+        raise RuntimeError(f"{lib_path} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(lib_path)
+    vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
+    lib.fa4_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+    lib.fa4_fwd.restype = i32
+    lib.fa4_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                               ctypes.POINTER(_Options), vp]
+    lib.fa4_fwd_ex.restype = i32
+    lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
+    lib.fa4_fwd_default_options.restype = None
+    lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
+    lib.fa4_device_status.restype = i32
+    lib.fa4_exp2_eval.argtypes = [vp, vp, vp, i64, vp]
+    lib.fa4_exp2_eval.restype = i32
+    lib.fa4_status_string.argtypes = [i32]
+    lib.fa4_status_string.restype = ctypes.c_char_p
+    lib.fa4_version.argtypes = []
+    lib.fa4_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().fa4_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load_library().fa4_version())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check(code: int, what: str) -> None:
+    if code != FA4_OK:
+        raise Fa4Error(code, what)
+
+
+def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
+             tau: float = 8.0, exp2_emulation: bool = True,
+             rescale_stats: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write attention forward into preallocated ``o`` and ``lse``.
+
+    Shapes: q, o [B,Sq,Hq,d]; k, v [B,Sk,Hkv,d] (BF16, contiguous, CUDA);
+    lse [B,Hq,Sq] fp32. ``scale`` defaults to 1/sqrt(d).
+    """
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,Sq,Hq,d] and k, v [B,Sk,Hkv,d]")
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("o must match q and lse must be [B,Hq,Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opt = _Options()
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    opt.tau = float(tau)
+    opt.exp2_emulation = 1 if exp2_emulation else 0
+    if rescale_stats is not None:
+        if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
+            raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")
+        opt.rescale_stats = rescale_stats.data_ptr()
+    code = lib.fa4_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
+                          ctypes.byref(opt), _stream_handle(stream))
+    _check(code, "fa4_fwd_ex")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: Optional[float] = None, **kw) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward; returns (o [B,Sq,Hq,d] BF16, lse [B,Hq,Sq] fp32)."""
+    B, Sq, Hq, _ = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    fwd_into(q, k, v, o, lse, causal, scale, **kw)
+    return o, lse
+
+
+def exp2_eval(x: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
+              ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The kernel's two 2^x paths on fp32 CUDA input: (emulated, MUFU.EX2)."""
+    lib = load_library()
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    y_emu = torch.empty_like(x)
+    y_mufu = torch.empty_like(x)
+    _check(lib.fa4_exp2_eval(x.data_ptr(), y_emu.data_ptr(), y_mufu.data_ptr(), x.numel(),
+                             _stream_handle(stream)), "fa4_exp2_eval")
+    return y_emu, y_mufu
+
+
+def device_status(clear: bool = True) -> Tuple[int, Tuple[int, int, int, int]]:
+    """Synchronise and read the kernels' status word: (code, detail[4])."""
+    lib = load_library()
+    detail = (ctypes.c_uint * 4)()
+    code = lib.fa4_device_status(1 if clear else 0, ctypes.byref(detail))
+    return int(code), tuple(int(x) for x in detail)

@@ -1,0 +1,253 @@
+// fa4_api.cu -- the C ABI declared in include/fa4.h: argument validation,
+// TMA tensor-map construction, kernel dispatch, the device status word and
+// the diagnostic 2^x evaluator.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa4.h"
+#include "fa4_internal.h"
+
+namespace fa4 {
+namespace {
+
+// Kernel-side status: [0] code, [1] role, [2] barrier id, [3] block.
+__device__ unsigned int g_status[4];
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_status for the current device (looked up once each).
+unsigned int* status_ptr(int dev) {
+  static std::atomic<unsigned int*> cache[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned int* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) return nullptr;
+  cache[dev].store(static_cast<unsigned int*>(addr), std::memory_order_release);
+  return static_cast<unsigned int*>(addr);
+}
+
+// [B, S, H, d] BF16 as a 4-D tensor (d, H, S, B); box = 64 columns x 128 rows
+// of one head, 128-byte swizzle (one swizzle row = 64 BF16).
+bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(H) * d * 2,
+                                 static_cast<cuuint64_t>(S) * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+fa4_status check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA4_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA4_ERR_UNSUPPORTED;
+  return FA4_OK;
+}
+
+__global__ void no_keys_kernel(uint4* o, int64_t n_vec, float* lse, int64_t n_lse) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_vec; i += stride)
+    o[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_lse; i += stride)
+    lse[i] = -INFINITY;
+}
+
+__global__ void exp2_eval_kernel(const float* x, float* y_emu, float* y_mufu, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
+    const float v = x[i];
+    y_emu[i] = ex2_emulated(v);
+    y_mufu[i] = ex2_mufu(v);
+  }
+}
+
+}  // namespace
+}  // namespace fa4
+
+extern "C" {
+
+void fa4_fwd_default_options(fa4_fwd_options* opt) {
+  if (!opt) return;
+  opt->tau = 8.0f;
+  opt->exp2_emulation = 1;
+  opt->rescale_stats = nullptr;
+}
+
+const char* fa4_status_string(fa4_status s) {
+  switch (s) {
+    case FA4_OK: return "FA4_OK";
+    case FA4_ERR_INVALID_ARG: return "FA4_ERR_INVALID_ARG";
+    case FA4_ERR_UNSUPPORTED: return "FA4_ERR_UNSUPPORTED";
+    case FA4_ERR_MISALIGNED: return "FA4_ERR_MISALIGNED";
+    case FA4_ERR_CUDA: return "FA4_ERR_CUDA";
+    case FA4_ERR_TIMEOUT: return "FA4_ERR_TIMEOUT";
+  }
+  return "FA4_ERR_UNKNOWN";
+}
+
+int fa4_version(void) { return 100; }
+
+fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                      const fa4_fwd_options* opt, fa4_stream_t stream) {
+  using namespace fa4;
+  fa4_fwd_options o_def;
+  fa4_fwd_default_options(&o_def);
+  const fa4_fwd_options& op = opt ? *opt : o_def;
+
+  // ---- arguments (nothing touches the GPU until they all pass)
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return FA4_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA4_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA4_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FA4_ERR_INVALID_ARG;
+  if (!std::isfinite(op.tau) || op.tau < 0.0f || op.tau > 64.0f) return FA4_ERR_INVALID_ARG;
+  if (op.exp2_emulation != 0 && op.exp2_emulation != 1) return FA4_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0) return FA4_OK;  // empty output: nothing to do
+  if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
+  auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (mis16(q) || mis16(o) || (Sk > 0 && (mis16(k) || mis16(v))) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return FA4_ERR_MISALIGNED;
+  if (op.rescale_stats && (reinterpret_cast<uintptr_t>(op.rescale_stats) & 7u) != 0)
+    return FA4_ERR_MISALIGNED;
+  const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
+  const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
+  const uint64_t lse_bytes = static_cast<uint64_t>(B) * Hq * Sq * 4;
+  if (overlaps(o, q_bytes, q, q_bytes) || overlaps(o, q_bytes, k, kv_bytes) ||
+      overlaps(o, q_bytes, v, kv_bytes) || overlaps(o, q_bytes, lse, lse_bytes) ||
+      overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+      overlaps(lse, lse_bytes, v, kv_bytes))
+    return FA4_ERR_INVALID_ARG;
+  const int64_t n_qblk = (static_cast<int64_t>(Sq) + 2 * kBM - 1) / (2 * kBM);
+  const int64_t grid = n_qblk * B * Hq;
+  if (grid > 0x7fffffffLL) return FA4_ERR_UNSUPPORTED;
+  // TMA limits: every global stride below 2^40 bytes.
+  if (static_cast<uint64_t>(Sq) * Hq * d * 2 >= (1ull << 40) ||
+      static_cast<uint64_t>(Sk) * Hkv * d * 2 >= (1ull << 40))
+    return FA4_ERR_UNSUPPORTED;
+
+  // ---- device
+  fa4_status st = check_device();
+  if (st != FA4_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
+  unsigned int* status = status_ptr(dev);
+  if (!status) return FA4_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (Sk == 0) {  // no keys: O = 0, LSE = -inf
+    no_keys_kernel<<<152, 256, 0, s>>>(static_cast<uint4*>(o), static_cast<int64_t>(q_bytes / 16),
+                                       lse, static_cast<int64_t>(lse_bytes / 4));
+    return cudaGetLastError() == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
+  }
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
+      !make_map(&tv, v, B, Sk, Hkv, d))
+    return FA4_ERR_CUDA;
+
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.n_qblk = static_cast<int>(n_qblk);
+  // Causal tiles run heaviest first across a chunk of heads whose K/V stay
+  // resident in L2; non-causal tiles of one head run side by side.
+  p.head_chunk = causal ? (B * Hq < 8 ? B * Hq : 8) : 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tau = op.tau;
+  p.stats = op.rescale_stats;
+  p.status = status;
+
+  const int emu = op.exp2_emulation ? 8 : 0;
+  cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu,
+                                               static_cast<unsigned>(grid), s)
+                              : launch_fwd_d128(tq, tk, tv, p, causal != 0, emu,
+                                                static_cast<unsigned>(grid), s);
+  return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
+}
+
+fa4_status fa4_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int d, float scale, int causal, fa4_stream_t stream) {
+  return fa4_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, nullptr, stream);
+}
+
+fa4_status fa4_device_status(int clear, unsigned int* detail) {
+  using namespace fa4;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA4_ERR_CUDA;
+  unsigned int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(h, g_status, sizeof h) != cudaSuccess) return FA4_ERR_CUDA;
+  if (detail) std::memcpy(detail, h, sizeof h);
+  if (clear) {
+    const unsigned int z[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_status, z, sizeof z) != cudaSuccess) return FA4_ERR_CUDA;
+  }
+  return h[0] == 0 ? FA4_OK : FA4_ERR_TIMEOUT;
+}
+
+fa4_status fa4_exp2_eval(const float* x, float* y_emu, float* y_mufu, int64_t n,
+                         fa4_stream_t stream) {
+  using namespace fa4;
+  if (n < 0) return FA4_ERR_INVALID_ARG;
+  if (n == 0) return FA4_OK;
+  if (!x || !y_emu || !y_mufu) return FA4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y_emu) |
+       reinterpret_cast<uintptr_t>(y_mufu)) & 3u)
+    return FA4_ERR_MISALIGNED;
+  fa4_status st = check_device();
+  if (st != FA4_OK) return st;
+  const int64_t blocks64 = (n + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(blocks64 < 152 * 8 ? blocks64 : 152 * 8);
+  exp2_eval_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y_emu, y_mufu, n);
+  return cudaGetLastError() == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,555 @@
+// fa4_fwd_kernel.cuh -- warp-specialised attention forward for sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) -- M = 256 rows
+// -- and walks every key block of 128 keys once ("FlashAttention-4:
+// Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware
+// Scaling", Table 1 / §3.1.1 tile M = 256, N = 128; §3.1.2 two output
+// tiles per CTA). Roles, one per warp group (§3.1.2, Method (1); "How
+// FlashAttention 4 Works", the Load / MMA / Softmax / Correction /
+// Epilogue split):
+//
+//   warps 0-3   softmax WG for tile 0: one thread owns one row (TMEM lane)
+//   warps 4-7   softmax WG for tile 1; both also run the epilogue
+//   warps 8-11  correction WG: rescales O in TMEM when a row group's
+//               reference max moves (conditional rescale, §3.1.4)
+//   warp 12     TMA load warp: Q once, then K_j / V_j into a ring of slots
+//   warp 13     MMA warp: one thread issues every tcgen05.mma
+//   warps 14-15 idle
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   S_t  = Q_t K_j^T   fp32, columns [128 t, 128 t + 128)
+//   P_t  (BF16, two per column) aliases the first 64 columns of S_t
+//   O_t  fp32, columns [256 + D t, 256 + D t + D)
+//
+// The MMA order per key block j is S_0, S_1 (both read K_j), then
+// O_0 += P_0 V_j, O_1 += P_1 V_j. Because P_t aliases S_t, S_t for block
+// j+1 is only issued once O_t += P_t V_j has completed.
+//
+// Every mbarrier wait is bounded (about half a second of globaltimer). On
+// expiry the waiting thread raises a CTA-wide abort flag and a device
+// status word; every role then leaves its loop, in-flight TMA copies and
+// MMAs are drained, and TMEM is freed before the CTA exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa4_exp2.cuh"
+#include "fa4_ptx.cuh"
+
+namespace fa4 {
+
+constexpr int kBM = 128;          // query rows per tile = TMEM lanes
+constexpr int kBN = 128;          // keys per block
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kWarpLoad = 12;
+constexpr int kWarpMma = 13;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+enum : unsigned { kStatusTimeout = 5u };
+enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3 };
+
+struct FwdParams {
+  __nv_bfloat16* o;            // [B, Sq, Hq, D]
+  float* lse;                  // [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Sk;
+  int group;                   // Hq / Hkv
+  int n_qblk;                  // ceil(Sq / 256)
+  int head_chunk;              // (b, h) pairs interleaved by the tile order
+  float scale_log2;            // scale * log2(e)
+  float tau;                   // rescale threshold, log2 units
+  unsigned long long* stats;   // optional rescale counters [2]
+  unsigned int* status;        // device status word [4]
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kTileBytes = kBM * D * 2;         // one 128 x D BF16 tile
+  static constexpr int kPanelBytes = kBM * 128;          // 128 rows x 128 B (64 columns)
+  static constexpr int kPanels = D / 64;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;      // K/V ring depth
+  static constexpr int kQ = 0;
+  static constexpr int kRing = kQ + 2 * kTileBytes;
+  static constexpr int kBars = kRing + kSlots * kTileBytes;
+  // barrier ids
+  static constexpr int bQ = 0;
+  static constexpr int bKvFull = 1;
+  static constexpr int bKvEmpty = bKvFull + kSlots;
+  static constexpr int bSFull = bKvEmpty + kSlots;       // [2]
+  static constexpr int bPFull = bSFull + 2;              // [2]
+  static constexpr int bOReady = bPFull + 2;             // [2]
+  static constexpr int bPvDone = bOReady + 2;            // [2]
+  static constexpr int bDrain = bPvDone + 2;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
+  static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
+  static constexpr int kMisc = kFlags + 8 * 4;           // tmem base, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;           // slack for 1 KB alignment
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+};
+
+// ------------------------------------------------------------ bounded waits
+struct Waiter {
+  volatile int* abort;
+  unsigned int* status;
+  unsigned role;
+
+  __device__ __forceinline__ bool slow(uint32_t bar, uint32_t parity, unsigned id,
+                                       bool honour_abort) const {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 63u) == 0u) {
+        if (honour_abort && *abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort = 1;
+          if (atomicCAS(status, 0u, kStatusTimeout) == 0u) {
+            status[1] = role;
+            status[2] = id;
+            status[3] = blockIdx.x;
+          }
+          __threadfence();
+          return false;
+        }
+      }
+    }
+  }
+  // Returns false if the CTA is aborting (this wait or another one expired).
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, unsigned id) const {
+    return mbar_try_wait(bar, parity) || slow(bar, parity, id, true);
+  }
+  // Used only while draining: waits for hardware-driven completions (TMA
+  // bytes, MMA commits) even after an abort, still bounded.
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, unsigned id) const {
+    return mbar_try_wait(bar, parity) || slow(bar, parity, id, false);
+  }
+};
+
+// ------------------------------------------------------------ tile geometry
+struct Tile {
+  int b, h, hk, q0;
+  int nkv[2];       // key blocks each query tile visits
+  int nkv_max;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Tile make_tile(const FwdParams& p) {
+  Tile tl;
+  const int n_bh = p.B * p.Hq;
+  const int per_chunk = p.head_chunk * p.n_qblk;
+  const int id = static_cast<int>(blockIdx.x);
+  const int chunk = id / per_chunk;
+  const int rem = id - chunk * per_chunk;
+  const int g_eff = min(p.head_chunk, n_bh - chunk * p.head_chunk);
+  const int qrank = rem / g_eff;
+  const int bh = chunk * p.head_chunk + (rem - qrank * g_eff);
+  // Causal: the largest query blocks (most key blocks) go first.
+  const int qb = CAUSAL ? (p.n_qblk - 1 - qrank) : qrank;
+  tl.b = bh / p.Hq;
+  tl.h = bh - tl.b * p.Hq;
+  tl.hk = tl.h / p.group;
+  tl.q0 = qb * 2 * kBM;
+  const int nblk = (p.Sk + kBN - 1) / kBN;
+  tl.nkv_max = 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = tl.q0 + t * kBM;
+    int n = 0;
+    if (r0 < p.Sq) {
+      if (CAUSAL) {
+        const int last_row = min(r0 + kBM - 1, p.Sq - 1);
+        const long long kmax = static_cast<long long>(last_row) + p.Sk - p.Sq;  // last allowed key
+        n = kmax < 0 ? 0 : min(nblk, static_cast<int>(kmax / kBN) + 1);
+      } else {
+        n = nblk;
+      }
+    }
+    tl.nkv[t] = n;
+    tl.nkv_max = max(tl.nkv_max, n);
+  }
+  return tl;
+}
+
+// ------------------------------------------------------------ load warp
+template <int D>
+__device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                          const CUtensorMap* tm_v, uint32_t sbase,
+                                          const Tile& tl, const Waiter& w) {
+  using L = Smem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  if (tl.nkv_max == 0) return;
+  mbar_arrive_expect_tx(bar(L::bQ), 2u * L::kTileBytes);
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int pn = 0; pn < L::kPanels; ++pn)
+      tma_load_4d(sbase + L::kQ + t * L::kTileBytes + pn * L::kPanelBytes, tm_q, bar(L::bQ),
+                  pn * 64, tl.h, tl.q0 + t * kBM, tl.b);
+  const int total = 2 * tl.nkv_max;   // K_0, V_0, K_1, V_1, ...
+  int issued = 0;
+  for (int idx = 0; idx < total; ++idx) {
+    const int s = idx % L::kSlots;
+    const uint32_t n = static_cast<uint32_t>(idx / L::kSlots);
+    if (!w.wait(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s)) break;
+    mbar_arrive_expect_tx(bar(L::bKvFull + s), L::kTileBytes);
+    const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
+    const int row = (idx >> 1) * kBN;
+#pragma unroll
+    for (int pn = 0; pn < L::kPanels; ++pn)
+      tma_load_4d(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm, bar(L::bKvFull + s),
+                  pn * 64, tl.hk, row, tl.b);
+    issued = idx + 1;
+  }
+  if (issued < total || *w.abort) {
+    // Let every copy this warp started land before the CTA frees its memory.
+    w.drain(bar(L::bQ), 0u, L::bQ);
+    for (int idx = max(0, issued - L::kSlots); idx < issued; ++idx) {
+      const int s = idx % L::kSlots;
+      w.drain(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u, L::bKvFull + s);
+    }
+  }
+}
+
+// ------------------------------------------------------------ MMA warp
+template <int D>
+__device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Tile& tl,
+                                         const Waiter& w) {
+  using L = Smem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major
+  const uint32_t col_s[2] = {L::kColS0, L::kColS1};
+  const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+  if (tl.nkv_max == 0) return;
+  bool ok = w.wait(bar(L::bQ), 0u, L::bQ);
+  tc_fence_after_sync();
+  for (int j = 0; ok && j < tl.nkv_max; ++j) {
+    // ---- S_t = Q_t K_j^T
+    const int ki = 2 * j, ks = ki % L::kSlots;
+    if (!(ok = w.wait(bar(L::bKvFull + ks), static_cast<uint32_t>(ki / L::kSlots) & 1u,
+                      L::bKvFull + ks)))
+      break;
+    tc_fence_after_sync();
+    const uint32_t k_s = sbase + L::kRing + ks * L::kTileBytes;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (j >= tl.nkv[t]) continue;
+      if (j > 0) {  // P_t (aliasing S_t) must be consumed before S_t is overwritten
+        if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t)))
+          break;
+        tc_fence_after_sync();
+      }
+      const uint32_t q_s = sbase + L::kQ + t * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+        mma_ss(tmem + col_s[t], smem_desc_sw128(q_s + off, 16, 1024),
+               smem_desc_sw128(k_s + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::bSFull + t));
+    }
+    if (!ok) break;
+    mma_commit(bar(L::bKvEmpty + ks));
+    // ---- O_t += P_t V_j
+    const int vi = 2 * j + 1, vs = vi % L::kSlots;
+    if (!(ok = w.wait(bar(L::bKvFull + vs), static_cast<uint32_t>(vi / L::kSlots) & 1u,
+                      L::bKvFull + vs)))
+      break;
+    tc_fence_after_sync();
+    const uint32_t v_s = sbase + L::kRing + vs * L::kTileBytes;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (j >= tl.nkv[t]) continue;
+      if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t)))
+        break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
+        mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
+               smem_desc_sw128(v_s + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar(L::bPvDone + t));
+    }
+    if (!ok) break;
+    mma_commit(bar(L::bKvEmpty + vs));
+  }
+  // Every MMA issued above has completed once this commit arrives.
+  mma_commit(bar(L::bDrain));
+  w.drain(bar(L::bDrain), 0u, L::bDrain);
+}
+
+// ------------------------------------------------------------ correction WG
+template <int D>
+__device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                                                const Tile& tl, const Waiter& w) {
+  using L = Smem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const float* alpha_s = reinterpret_cast<const float*>(smem + L::kAlpha);
+  const volatile int* flags_s = reinterpret_cast<const volatile int*>(smem + L::kFlags);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+  for (int j = 0; j < tl.nkv_max; ++j) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (j >= tl.nkv[t]) continue;
+      if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(j) & 1u, L::bPFull + t)) return;
+      tc_fence_after_sync();
+      if (j > 0 && flags_s[t * 4 + wq] != 0) {
+        if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t))
+          return;
+        tc_fence_after_sync();
+        const float a = alpha_s[t * kBM + r];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          const uint32_t addr = lane_base + col_o[t] + c * 32;
+          tmem_ld_x32(addr, x);
+          tmem_wait_ld_x32(x);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * a);
+          tmem_st_x32(addr, x);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::bOReady + t));
+    }
+  }
+}
+
+// ------------------------------------------------------------ softmax WGs
+// Column c of a 128-key block goes through the software 2^x when
+// c % PERIOD == PERIOD - 1 (PERIOD = 8: 12.5 % of the entries); PERIOD = 0
+// sends every entry through MUFU.EX2.
+template <int PERIOD>
+__host__ __device__ constexpr bool emulated_column(int c) {
+  if constexpr (PERIOD <= 0) {
+    return false;
+  } else {
+    return (c % PERIOD) == PERIOD - 1;
+  }
+}
+
+template <int D, bool CAUSAL, int EMU_PERIOD>
+__device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                                             const Tile& tl, const FwdParams& p,
+                                             const Waiter& w) {
+  using L = Smem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;                 // row within the tile = TMEM lane
+  const int row = tl.q0 + t * kBM + r;          // query index
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlpha);
+  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + L::kFlags);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t s_addr = lane_base + (t == 0 ? L::kColS0 : L::kColS1);
+  const uint32_t o_addr = lane_base + (t == 0 ? L::kColO0 : L::kColO1);
+  const int n = tl.nkv[t];
+  const float cl2 = p.scale_log2;
+  // Keys k < lim_row are visible to this row; lim_min is the tile's smallest.
+  const int shift = p.Sk - p.Sq;
+  const int lim_row = CAUSAL ? max(0, min(p.Sk, row + shift + 1)) : p.Sk;
+  const int row_min = tl.q0 + t * kBM;
+  const int lim_min = CAUSAL ? max(0, min(p.Sk, row_min + shift + 1)) : p.Sk;
+
+  float m_ref = -INFINITY;      // reference max (log2 units) of the last rescale
+  float l = 0.0f;               // running sum of p relative to m_ref
+  unsigned n_rescaled = 0, n_steps = 0;
+  bool ok = true;
+
+  for (int j = 0; j < n; ++j) {
+    if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(j) & 1u, L::bSFull + t))) break;
+    tc_fence_after_sync();
+    uint32_t s[128];
+    tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    float v[128];
+#pragma unroll
+    for (int c = 0; c < 128; ++c) v[c] = __uint_as_float(s[c]);
+    if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
+      const int lim = lim_row - j * kBN;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) v[c] = (c < lim) ? v[c] : -INFINITY;
+    }
+    // block max of the raw scores (scale > 0, so max commutes with it)
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = v[i];
+#pragma unroll
+    for (int c = 8; c < 128; c += 8)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], v[c + i]);
+    const float m_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    const float m_blk = m_raw * cl2;
+    const float m_cand = fmaxf(m_ref, m_blk);
+    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by > tau,
+    // decided for the whole warp so the correction stays warp-uniform.
+    const bool need = m_cand > m_ref + p.tau;
+    const bool warp_need = __any_sync(0xffffffffu, need);
+    if (warp_need) {
+      const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+      l *= alpha;
+      if (m_cand != -INFINITY) m_ref = m_cand;
+      alpha_s[t * kBM + r] = alpha;
+      if (j > 0) ++n_rescaled;
+    }
+    if (j > 0) ++n_steps;
+    if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+    const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+    // p = 2^(c*s - m_ref); part of the entries through the FMA-pipe
+    // emulation (§3.1.3), the rest through MUFU.EX2.
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+      const float x0 = fmaf(v[c], cl2, neg_m);
+      const float x1 = fmaf(v[c + 1], cl2, neg_m);
+      const bool emu0 = emulated_column<EMU_PERIOD>(c);
+      const bool emu1 = emulated_column<EMU_PERIOD>(c + 1);
+      const float p0 = emu0 ? ex2_emulated(x0) : ex2_mufu(x0);
+      const float p1 = emu1 ? ex2_emulated(x1) : ex2_mufu(x1);
+      acc[(c >> 1) & 3] += p0 + p1;
+      pk[c >> 1] = pack_bf16x2(p0, p1);
+    }
+    l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    tmem_st_x32(s_addr + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+    tmem_st_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+    tmem_wait_st();
+    tc_fence_before_sync();
+    mbar_arrive(bar(L::bPFull + t));
+  }
+
+  // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l)
+  if (ok && n > 0) {
+    ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n - 1) & 1u, L::bPvDone + t);
+    tc_fence_after_sync();
+  }
+  if (!ok) return;
+  const bool row_valid = row < p.Sq;
+  const bool has_keys = n > 0 && m_ref != -INFINITY;
+  const float inv_l = has_keys ? 1.0f / l : 0.0f;
+  __nv_bfloat16* orow =
+      p.o + ((static_cast<int64_t>(tl.b) * p.Sq + row) * p.Hq + tl.h) * static_cast<int64_t>(D);
+  if (n > 0) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t x[32];
+      tmem_ld_x32(o_addr + c * 32, x);
+      tmem_wait_ld_x32(x);
+      if (row_valid) {
+        uint32_t pkd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pkd[i] = pack_bf16x2(__uint_as_float(x[2 * i]) * inv_l, __uint_as_float(x[2 * i + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+      }
+    }
+  } else if (row_valid) {
+    uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (row_valid) {
+    p.lse[(static_cast<int64_t>(tl.b) * p.Hq + tl.h) * p.Sq + row] =
+        has_keys ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  }
+  if (p.stats != nullptr && lane == 0 && n_steps > 0) {
+    atomicAdd(&p.stats[0], static_cast<unsigned long long>(n_rescaled));
+    atomicAdd(&p.stats[1], static_cast<unsigned long long>(n_steps));
+  }
+}
+
+// ------------------------------------------------------------ kernel
+template <int D, bool CAUSAL, int EMU_PERIOD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const Tile tl = make_tile<CAUSAL>(p);
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    mbar_init(bar(L::bQ), 1);
+    for (int s = 0; s < L::kSlots; ++s) {
+      mbar_init(bar(L::bKvFull + s), 1);
+      mbar_init(bar(L::bKvEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::bSFull + t), 1);
+      mbar_init(bar(L::bPFull + t), kBM);
+      mbar_init(bar(L::bOReady + t), kBM);
+      mbar_init(bar(L::bPvDone + t), 1);
+    }
+    mbar_init(bar(L::bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    regs_increase<184>();
+    const Waiter w{abort_flag, p.status, kRoleSoftmax};
+    softmax_role<D, CAUSAL, EMU_PERIOD>(warp >> 2, sbase, smem, tmem, tl, p, w);
+  } else if (warp < 12) {
+    regs_decrease<80>();
+    const Waiter w{abort_flag, p.status, kRoleCorrection};
+    correction_role<D>(sbase, smem, tmem, tl, w);
+  } else {
+    regs_decrease<64>();
+    if (warp == kWarpLoad && lane == 0) {
+      const Waiter w{abort_flag, p.status, kRoleLoad};
+      load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, w);
+    } else if (warp == kWarpMma && lane == 0) {
+      const Waiter w{abort_flag, p.status, kRoleMma};
+      mma_role<D>(sbase, tmem, tl, w);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa4

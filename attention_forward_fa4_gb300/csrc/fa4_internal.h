@@ -1,0 +1,20 @@
+// fa4_internal.h -- host-side declarations shared by the library's
+// translation units (one per head dimension, plus the C-ABI layer).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa4_fwd_kernel.cuh"
+
+namespace fa4 {
+
+// Enqueue the forward kernel for head dim 64 / 128. `emu_period` is 0
+// (MUFU.EX2 only) or 8 (one entry in 8 through the software 2^x).
+cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdParams& p, bool causal, int emu_period, unsigned grid,
+                           cudaStream_t stream);
+cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, bool causal, int emu_period, unsigned grid,
+                            cudaStream_t stream);
+
+}  // namespace fa4

@@ -1,0 +1,133 @@
+/*
+ * fa4.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The operation is exact attention forward with a per-row logsumexp,
+ * computed tile by tile with an online softmax so that the score matrix S
+ * and the probabilities P never reach HBM. It is the forward pass described
+ * in "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+ * Asymmetric Hardware Scaling" (Method; §3.1.1-§3.1.4; Table 1, Table 2,
+ * Eq. 6) and "How FlashAttention 4 Works" (warp roles, TMA load warp,
+ * lazy rescale, cubic 2^x approximation).
+ *
+ * For every batch b, query head h and query row i, with kv head
+ * g = h / (Hq / Hkv):
+ *     x_j       = scale * <q[b,i,h,:], k[b,j,g,:]>
+ *     valid(j)  = !causal || j <= i + (Sk - Sq)      (bottom-right causal)
+ *     O[b,i,h,:] = sum_{valid j} exp(x_j - m) v[b,j,g,:] / sum_{valid j} exp(x_j - m)
+ *     LSE[b,h,i] = m + ln sum_{valid j} exp(x_j - m),   m = max_{valid j} x_j
+ * A row with no valid key gets O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense and contiguous: q, o [B, Sq, Hq, d] BF16;
+ *     k, v [B, Sk, Hkv, d] BF16; lse [B, Hq, Sq] fp32 (natural log).
+ *   - Pointers are DEVICE pointers owned by the caller; the library keeps
+ *     none of them after the call returns and allocates no device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). They validate their arguments first and launch
+ *     nothing when validation fails.
+ *   - Kernel waits are bounded. A pipeline stage that stalls for longer
+ *     than its limit makes the kernel give up cleanly and record
+ *     FA4_ERR_TIMEOUT in a per-device status word that fa4_device_status()
+ *     reads; the CUDA context stays usable.
+ *   - All functions are thread-safe.
+ */
+#ifndef FA4_H_
+#define FA4_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t. */
+typedef struct CUstream_st *fa4_stream_t;
+
+typedef enum {
+    FA4_OK = 0,
+    FA4_ERR_INVALID_ARG = 1,  /* null pointer, bad size, aliasing, bad scale   */
+    FA4_ERR_UNSUPPORTED = 2,  /* head dim not in {64,128}; device not cc 10.3  */
+    FA4_ERR_MISALIGNED = 3,   /* q/k/v/o not 16-byte aligned, lse not 4-byte   */
+    FA4_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed              */
+    FA4_ERR_TIMEOUT = 5       /* a kernel pipeline wait ran out (device status) */
+} fa4_status;
+
+/* Options of fa4_fwd_ex. Fill with fa4_fwd_default_options() first. */
+typedef struct {
+    /* Conditional-rescale threshold in log2 units ("FlashAttention-4",
+     * §3.1.4, Eq. 6): the running output is only rescaled when a row's new
+     * block maximum exceeds the reference maximum by more than tau.
+     * 8.0 (= log2 256) is the default; 0.0 gives the eager online softmax.
+     * Must be finite and in [0, 64]. */
+    float tau;
+    /* Software 2^x beside MUFU.EX2 ("FlashAttention-4", §3.1.3): 1 runs a
+     * Cody-Waite + degree-3 Horner polynomial on 1/8 of the softmax entries,
+     * 0 sends every entry through MUFU.EX2. */
+    int exp2_emulation;
+    /* Optional DEVICE pointer to two uint64 counters, or NULL. When set, the
+     * kernel adds [0] += number of (32-row group, key block) steps that
+     * rescaled the output, [1] += number of such steps after the first key
+     * block of each tile. The caller zeroes them. */
+    unsigned long long *rescale_stats;
+} fa4_fwd_options;
+
+/* Default options: tau = 8, exp2_emulation = 1, rescale_stats = NULL. */
+void fa4_fwd_default_options(fa4_fwd_options *opt);
+
+/*
+ * fa4_fwd -- attention forward with default options.
+ *
+ *   q      [B, Sq, Hq, d]  BF16, device, 16-byte aligned
+ *   k, v   [B, Sk, Hkv, d] BF16, device, 16-byte aligned
+ *   o      [B, Sq, Hq, d]  BF16, device, 16-byte aligned, written
+ *   lse    [B, Hq, Sq]     fp32, device, 4-byte aligned, written
+ *   B, Sq, Sk >= 0 (B*Sq == 0 is a no-op; Sk == 0 gives O = 0, LSE = -inf);
+ *   Hq, Hkv >= 1 with Hq % Hkv == 0; d in {64, 128};
+ *   scale finite and > 0 (usually 1/sqrt(d)); causal 0 or 1.
+ *   o and lse must not overlap q, k, v or each other.
+ *
+ * Returns FA4_OK after the kernel is enqueued, or an error code with
+ * nothing launched.
+ */
+fa4_status fa4_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                   int causal, fa4_stream_t stream);
+
+/* fa4_fwd with explicit options (opt may be NULL for the defaults). */
+fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                      int causal, const fa4_fwd_options *opt, fa4_stream_t stream);
+
+/*
+ * fa4_device_status -- synchronise the current device and return the
+ * kernel-side status word: FA4_OK, or FA4_ERR_TIMEOUT if any kernel of
+ * this library gave up on a pipeline wait since the last clear. `detail`
+ * (may be NULL) receives 4 words: the error code, the waiting role
+ * (0 load, 1 mma, 2 softmax, 3 correction), the barrier id and the block
+ * index. When `clear` is non-zero the word is reset to FA4_OK.
+ * Returns FA4_ERR_CUDA if the device cannot be reached.
+ */
+fa4_status fa4_device_status(int clear, unsigned int *detail);
+
+/*
+ * fa4_exp2_eval -- diagnostic: evaluate the kernel's two 2^x paths on n
+ * fp32 inputs: y_emu[i] = Cody-Waite + degree-3 polynomial emulation,
+ * y_mufu[i] = MUFU.EX2 (ex2.approx.ftz.f32). All three pointers are device
+ * fp32 arrays of n elements (n >= 0). This is the kernel's own device
+ * function ("FlashAttention-4", §3.1.3, Table 2), exported so it can be
+ * checked exhaustively over every BF16 input.
+ */
+fa4_status fa4_exp2_eval(const float *x, float *y_emu, float *y_mufu, int64_t n,
+                         fa4_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *fa4_status_string(fa4_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA4_H_ */

@@ -1,0 +1,99 @@
+"""The C-ABI library loads without a GPU, exports every function that
+include/fa4.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_fa4_gb300 import build
+    build.build()
+    import attention_forward_fa4_gb300 as fa4
+    return fa4.load_library()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fa4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "fa4_fwd" in names and "fa4_fwd_ex" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for code, name in enumerate(["FA4_OK", "FA4_ERR_INVALID_ARG", "FA4_ERR_UNSUPPORTED",
+                                 "FA4_ERR_MISALIGNED", "FA4_ERR_CUDA", "FA4_ERR_TIMEOUT"]):
+        assert lib.fa4_status_string(code).decode() == name
+    assert lib.fa4_version() >= 100
+
+
+P = 0x100000          # aligned stand-in addresses: never dereferenced on failure paths
+Q, K, V, O, L = P, 2 * P, 3 * P, 4 * P, 5 * P
+
+
+def _call(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, Hq=2, Hkv=2, Sq=64, Sk=64, d=64, scale=0.125,
+          causal=0):
+    return lib.fa4_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, None)
+
+
+def test_argument_errors_launch_nothing(lib):
+    import attention_forward_fa4_gb300 as fa4
+    assert _call(lib, q=0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, o=0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, lse=0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, k=0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, Hq=3, Hkv=2) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, Hkv=0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, B=-1) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, Sk=-5) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, scale=0.0) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, scale=float("nan")) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, causal=2) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, d=96) == fa4.FA4_ERR_UNSUPPORTED
+    assert _call(lib, d=256) == fa4.FA4_ERR_UNSUPPORTED
+    assert _call(lib, q=Q + 8) == fa4.FA4_ERR_MISALIGNED
+    assert _call(lib, v=V + 2) == fa4.FA4_ERR_MISALIGNED
+    assert _call(lib, lse=L + 2) == fa4.FA4_ERR_MISALIGNED
+    # o overlapping q, lse overlapping v
+    assert _call(lib, o=Q + 16) == fa4.FA4_ERR_INVALID_ARG
+    assert _call(lib, lse=V) == fa4.FA4_ERR_INVALID_ARG
+
+
+def test_empty_problems_are_no_ops(lib):
+    import attention_forward_fa4_gb300 as fa4
+    assert _call(lib, B=0, q=0, k=0, v=0, o=0, lse=0) == fa4.FA4_OK
+    assert _call(lib, Sq=0, q=0, o=0, lse=0) == fa4.FA4_OK
+
+
+def test_options_are_validated(lib):
+    import attention_forward_fa4_gb300 as fa4
+    from attention_forward_fa4_gb300 import _Options
+    opt = _Options()
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    assert opt.tau == 8.0 and opt.exp2_emulation == 1 and not opt.rescale_stats
+    for tau in (-1.0, float("inf"), 100.0):
+        opt.tau = tau
+        assert lib.fa4_fwd_ex(Q, K, V, O, L, 1, 2, 2, 64, 64, 64, 0.125, 0, ctypes.byref(opt),
+                              None) == fa4.FA4_ERR_INVALID_ARG
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    opt.exp2_emulation = 3
+    assert lib.fa4_fwd_ex(Q, K, V, O, L, 1, 2, 2, 64, 64, 64, 0.125, 0, ctypes.byref(opt),
+                          None) == fa4.FA4_ERR_INVALID_ARG
+
+
+def test_without_a_device_valid_calls_report_cuda_error(lib):
+    import torch
+    import attention_forward_fa4_gb300 as fa4
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(lib) in (fa4.FA4_ERR_CUDA, fa4.FA4_ERR_UNSUPPORTED)
