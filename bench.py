@@ -1,0 +1,393 @@
+"""Benchmark of the GB300 attention forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--tau T] [--no-emu]
+
+One step = one attention forward over the workload's synthetic BF16 input
+(default: B=2, Hq=Hkv=16, Sq=Sk=8192, d=128, causal). ``value`` is the
+whole-job TFLOP/s (4*B*Hq*Sq*Sk*d, halved for causal) from CUDA events
+around each launch, with the inputs resident in HBM and L2 flushed before
+every timed launch. ``e2e`` is the same metric with the host->device copy
+of q, k, v and the device->host copy of o and lse inside each step.
+
+Under torchrun (N > 1) each rank runs its own shard of a global batch
+(weak scaling, no collective on the data path); time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(rank 0 only), each step a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+from typing import Dict, List, Optional, Tuple
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of 2.25 PFLOP/s roofline"
+NOMINAL_BF16_TFLOPS = 2250.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_NAME = "fa4_fwd_kernel"
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env() -> Tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_workload(w: workloads.Workload, rank: int, world: int) -> Tuple[workloads.Workload, int]:
+    """Weak scaling: every rank owns B batches of a global batch of B*world.
+
+    Returns the per-rank workload and the batch offset of its shard (used to
+    seed distinct data per shard)."""
+    if world < 1 or not (0 <= rank < world):
+        raise ValueError("bad rank/world")
+    return w, rank * w.B
+
+
+def max_over_ranks(values: List[float], dist, device) -> List[float]:
+    """Element-wise max of per-rank timings (the job is as slow as its
+    slowest rank)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def kernel_sources_hash() -> str:
+    """Hash of the kernel sources; a stored ncu traffic figure only applies
+    to the build it was measured on."""
+    csrc = os.path.join(ROOT, "attention_forward_fa4_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload_name: str) -> Optional[dict]:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_sources_hash:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_sources_hash():
+        return None
+    return {"bytes": float(m_b.group(1)), "source": os.path.relpath(path, ROOT)}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "_source": "fallback"}
+
+
+def table1_cycles(M: int, N: int, d: int, flops_per_clk: float = 8192.0,
+                  exp_per_clk: float = 16.0, smem_bytes_per_clk: float = 128.0) -> dict:
+    """Closed-form forward roofline per key block ("FlashAttention-4", Table 1,
+    §3.1.1): MMA = 4*M*N*d / F; exp = M*N / MUFU rate; SMEM = bytes of the
+    operands read from shared memory by the MMAs / SMEM bandwidth. Each
+    128-row slice of the M rows reads Q, K and V (N x d BF16 each)."""
+    mma = 4.0 * M * N * d / flops_per_clk
+    exp = M * N / exp_per_clk
+    smem = (M // 128) * 3 * N * d * 2 / smem_bytes_per_clk
+    return {"mma": mma, "exp": exp, "smem": smem}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> Optional[dict]:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5], parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return None
+        sm = sorted(r[1] for r in inside)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for name, flag in zip(names, r[4]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_rate(w: workloads.Workload, q, k, v, seconds: float, seed: int = 0
+                ) -> Tuple[float, float, int, str]:
+    """Time the fp64 oracle on a seeded random row sample sized for about
+    ``seconds`` of host work; returns (flop/s, flops done, threads, sample)."""
+    import numpy as np
+    from oracle import attn as oracle
+
+    def flops_of(rows):
+        i = rows % w.Sq
+        keys = np.minimum(w.Sk, i + (w.Sk - w.Sq) + 1) if w.causal else np.full(rows.shape, w.Sk)
+        return float(4.0 * w.d * np.maximum(keys, 0).sum())
+
+    rng = np.random.default_rng(seed + 12345)
+    total_rows = w.B * w.Hq * w.Sq
+    probe = rng.integers(0, total_rows, size=16, dtype=np.int64)
+    t = time.perf_counter()
+    oracle.attention_fwd_rows(q, k, v, w.scale, w.causal, probe)
+    dt = max(time.perf_counter() - t, 1e-4)
+    n = int(max(16, min(total_rows, 16 * seconds / dt)))
+    rows = np.sort(rng.integers(0, total_rows, size=n, dtype=np.int64))
+    t = time.perf_counter()
+    oracle.attention_fwd_rows(q, k, v, w.scale, w.causal, rows)
+    dt = time.perf_counter() - t
+    f = flops_of(rows)
+    return f / dt, f, oracle.num_threads(), f"{n} seeded random query rows of {total_rows}"
+
+
+def run_reference(args, w: workloads.Workload) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import build as oracle_build
+    oracle_build.build()
+    q, k, v = workloads.make_inputs(w, seed=0)
+    per_step_s = max(0.2, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_rate(w, q, k, v, per_step_s, seed=1000 + i)
+    flops = 0.0
+    secs = 0.0
+    threads = 1
+    sample = ""
+    for i in range(args.steps):
+        rate, f, threads, sample = oracle_rate(w, q, k, v, per_step_s, seed=i)
+        flops += f
+        secs += f / rate
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), sample_per_step=sample),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args, w: workloads.Workload) -> None:
+    import torch
+
+    rank, world, local_rank = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    import attention_forward_fa4_gb300 as fa4
+    fa4.load_library()
+
+    w_rank, batch_offset = shard_workload(w, rank, world)
+    q_h, k_h, v_h = workloads.make_inputs(w_rank, seed=0, batch_offset=batch_offset)
+    stream = torch.cuda.Stream(device=dev)
+    q = q_h.to(dev)
+    k = k_h.to(dev)
+    v = v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kw = dict(tau=args.tau, exp2_emulation=not args.no_emu)
+
+    def launch():
+        fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            launch()
+    torch.cuda.synchronize()
+    code, detail = fa4.device_status(clear=True)
+    if code != fa4.FA4_OK:
+        raise SystemExit(f"kernel status {fa4.status_string(code)} {detail}")
+
+    # ---- device-timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    time.sleep(0.3 if sampler else 0.0)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()                       # evict q/k/v/o from L2 between launches
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    code, detail = fa4.device_status(clear=True)
+    if code != fa4.FA4_OK:
+        raise SystemExit(f"kernel status {fa4.status_string(code)} {detail}")
+
+    # ---- end to end: pinned host inputs in, host outputs out, every step
+    q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    o_p = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lse_p = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e2e_steps):
+            q.copy_(q_p, non_blocking=True)
+            k.copy_(k_p, non_blocking=True)
+            v.copy_(v_p, non_blocking=True)
+            launch()
+            o_p.copy_(o, non_blocking=True)
+            lse_p.copy_(lse, non_blocking=True)
+        e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    if pg:
+        kernel_ms, e2e_ms = max_over_ranks([kernel_ms, e2e_ms], pg, dev)
+
+    flops_rank_step = w_rank.flops
+    value = flops_rank_step * args.steps * world / (kernel_ms * 1e-3) / 1e12
+    e2e_value = flops_rank_step * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    per_launch_ms = kernel_ms / args.steps
+    achieved = flops_rank_step / (per_launch_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    traffic = stored_traffic(w.name)
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, _, threads, sample = oracle_rate(w, q_h, k_h, v_h, args.cpu_seconds)
+            cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": sample}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_launch_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(w.describe(), global_batch=w.B * world, parallelism=f"replica-shards{world}",
+                           l2="flushed before every timed launch (256 MiB write)",
+                           tau=args.tau, exp2_emulation=not args.no_emu),
+            "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peaks['_source']} bf16_tflops (burst)",
+                         "traffic": traffic["bytes"] if traffic else None,
+                         "traffic_source": traffic["source"] if traffic else None,
+                         "algorithmic_bytes": w_rank.hbm_bytes},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main(argv: Optional[List[str]] = None) -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.LONG_CAUSAL.name,
+                    choices=[x.name for x in workloads.ALL_NAMED])
+    ap.add_argument("--tau", type=float, default=8.0)
+    ap.add_argument("--no-emu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = workloads.by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
