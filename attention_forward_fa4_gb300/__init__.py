@@ -46,7 +46,15 @@ class Fa4Error(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("exp2_emulation", ctypes.c_int),
-                ("rescale_stats", ctypes.c_void_p)]
+                ("rescale_stats", ctypes.c_void_p), ("trace", ctypes.c_void_p),
+                ("trace_ctas", ctypes.c_int)]
+
+
+TRACE_EVENTS = 10
+TRACE_STEPS = 128
+TRACE_EVENT_NAMES = ("mma_s_wait", "mma_s_issued", "mma_pv_wait", "mma_pv_issued",
+                     "sm_s_ready", "sm_loaded", "sm_exp_done", "sm_arrived",
+                     "co_wake", "co_arrived")
 
 
 def load_library():
@@ -100,6 +108,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
              tau: float = 8.0, exp2_emulation: bool = True,
              rescale_stats: Optional[torch.Tensor] = None,
+             trace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> None:
     """Write attention forward into preallocated ``o`` and ``lse``.
 
@@ -132,6 +141,13 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
             raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")
         opt.rescale_stats = rescale_stats.data_ptr()
+    if trace is not None:
+        per_cta = TRACE_EVENTS * TRACE_STEPS * 2
+        if trace.dtype != torch.int64 or not trace.is_cuda or trace.numel() % per_cta:
+            raise ValueError("trace must be a CUDA int64 tensor of n_ctas * "
+                             f"{per_cta} elements")
+        opt.trace = trace.data_ptr()
+        opt.trace_ctas = trace.numel() // per_cta
     code = lib.fa4_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
                           ctypes.byref(opt), _stream_handle(stream))

@@ -94,12 +94,20 @@ __global__ void no_keys_kernel(uint4* o, int64_t n_vec, float* lse, int64_t n_ls
     lse[i] = -INFINITY;
 }
 
+// Evaluates the softmax's own paired emulation (ex2_emulated2) two inputs
+// at a time, and MUFU.EX2 on each input.
 __global__ void exp2_eval_kernel(const float* x, float* y_emu, float* y_mufu, int64_t n) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
-    const float v = x[i];
-    y_emu[i] = ex2_emulated(v);
-    y_mufu[i] = ex2_mufu(v);
+  const int64_t pairs = (n + 1) / 2;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < pairs; i += stride) {
+    const int64_t a = 2 * i, b = (2 * i + 1 < n) ? 2 * i + 1 : 2 * i;
+    const float2 y = ex2_emulated2(make_float2(x[a], x[b]));
+    y_emu[a] = y.x;
+    y_mufu[a] = ex2_mufu(x[a]);
+    if (b != a) {
+      y_emu[b] = y.y;
+      y_mufu[b] = ex2_mufu(x[b]);
+    }
   }
 }
 
@@ -113,6 +121,8 @@ void fa4_fwd_default_options(fa4_fwd_options* opt) {
   opt->tau = 8.0f;
   opt->exp2_emulation = 1;
   opt->rescale_stats = nullptr;
+  opt->trace = nullptr;
+  opt->trace_ctas = 0;
 }
 
 const char* fa4_status_string(fa4_status s) {
@@ -153,6 +163,8 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
     return FA4_ERR_MISALIGNED;
   if (op.rescale_stats && (reinterpret_cast<uintptr_t>(op.rescale_stats) & 7u) != 0)
     return FA4_ERR_MISALIGNED;
+  if (op.trace && (reinterpret_cast<uintptr_t>(op.trace) & 7u) != 0) return FA4_ERR_MISALIGNED;
+  if (op.trace && op.trace_ctas < 0) return FA4_ERR_INVALID_ARG;
   const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
   const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
   const uint64_t lse_bytes = static_cast<uint64_t>(B) * Hq * Sq * 4;
@@ -206,6 +218,8 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.tau = op.tau;
   p.stats = op.rescale_stats;
   p.status = status;
+  p.trace = op.trace;
+  p.trace_ctas = op.trace ? op.trace_ctas : 0;
 
   const int emu = op.exp2_emulation ? 8 : 0;
   cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu,

@@ -1,5 +1,6 @@
 // fa4_fwd_d64.cu -- instantiations of the forward kernel for head dim 64
-// (causal / non-causal x MUFU-only / partial software 2^x).
+// (causal / non-causal x MUFU-only / one entry pair in 8 through the
+// software 2^x).
 #include "fa4_internal.h"
 
 namespace fa4 {

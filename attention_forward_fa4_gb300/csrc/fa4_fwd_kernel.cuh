@@ -11,7 +11,9 @@
 //   warps 0-3   softmax WG for tile 0: one thread owns one row (TMEM lane)
 //   warps 4-7   softmax WG for tile 1; both also run the epilogue
 //   warps 8-11  correction WG: rescales O in TMEM when a row group's
-//               reference max moves (conditional rescale, §3.1.4)
+//               reference max moves (conditional rescale, §3.1.4); groups
+//               that need no rescale never wait for it
+
 //   warp 12     TMA load warp: Q once, then K_j / V_j into a ring of slots
 //   warp 13     MMA warp: one thread issues every tcgen05.mma
 //   warps 14-15 idle
@@ -61,7 +63,40 @@ struct FwdParams {
   float tau;                   // rescale threshold, log2 units
   unsigned long long* stats;   // optional rescale counters [2]
   unsigned int* status;        // device status word [4]
+  unsigned long long* trace;   // optional per-role cycle trace (see trace_mark)
+  int trace_ctas;              // CTAs (by blockIdx.x) that record a trace
 };
+
+// ------------------------------------------------------------ cycle trace
+// Optional diagnostic: when FwdParams::trace is set, CTAs with
+// blockIdx.x < trace_ctas record the SM cycle counter at fixed points of
+// each role, for key block j < kTraceSteps and query tile t:
+//   trace[((cta * kTraceEvents + event) * kTraceSteps + j) * 2 + t].
+// The MMA thread, lane 0 of the first softmax warp of each tile and lane 0
+// of the first correction warp record. A null pointer costs one uniform
+// branch per event.
+constexpr int kTraceSteps = 128;
+enum TraceEvent : int {
+  kTrMmaSWait = 0,     // MMA: starts waiting for the S_t slot / K_j
+  kTrMmaSIssued,       // MMA: S_t = Q_t K_j^T issued and committed
+  kTrMmaPvWait,        // MMA: starts waiting for o_ready[t]
+  kTrMmaPvIssued,      // MMA: O_t += P_t V_j issued and committed
+  kTrSmSReady,         // softmax: S_t visible (s_full passed)
+  kTrSmLoaded,         // softmax: S row in registers
+  kTrSmExpDone,        // softmax: P computed and packed
+  kTrSmArrived,        // softmax: P stored, barrier arrived
+  kTrCoWake,           // correction: p_full passed
+  kTrCoArrived,        // correction: o_ready arrived
+  kTraceEvents
+};
+
+__device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, int t) {
+  if (p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas && j < kTraceSteps) {
+    uint64_t c;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+    p.trace[((static_cast<size_t>(blockIdx.x) * kTraceEvents + ev) * kTraceSteps + j) * 2 + t] = c;
+  }
+}
 
 template <int D>
 struct Smem {
@@ -80,7 +115,8 @@ struct Smem {
   static constexpr int bPFull = bSFull + 2;              // [2]
   static constexpr int bOReady = bPFull + 2;             // [2]
   static constexpr int bPvDone = bOReady + 2;            // [2]
-  static constexpr int bDrain = bPvDone + 2;
+  static constexpr int bCDone = bPvDone + 2;             // [2]
+  static constexpr int bDrain = bCDone + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
   static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
@@ -216,7 +252,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // ------------------------------------------------------------ MMA warp
 template <int D>
 __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Tile& tl,
-                                         const Waiter& w) {
+                                         const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
@@ -237,6 +273,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (j >= tl.nkv[t]) continue;
+      trace_mark(p, kTrMmaSWait, j, t);
       if (j > 0) {  // P_t (aliasing S_t) must be consumed before S_t is overwritten
         if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t)))
           break;
@@ -250,6 +287,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
                smem_desc_sw128(k_s + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
       }
       mma_commit(bar(L::bSFull + t));
+      trace_mark(p, kTrMmaSIssued, j, t);
     }
     if (!ok) break;
     mma_commit(bar(L::bKvEmpty + ks));
@@ -263,6 +301,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (j >= tl.nkv[t]) continue;
+      trace_mark(p, kTrMmaPvWait, j, t);
       if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t)))
         break;
       tc_fence_after_sync();
@@ -274,6 +313,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
                (j > 0 || kk > 0) ? 1u : 0u);
       }
       mma_commit(bar(L::bPvDone + t));
+      trace_mark(p, kTrMmaPvIssued, j, t);
     }
     if (!ok) break;
     mma_commit(bar(L::bKvEmpty + vs));
@@ -286,7 +326,8 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
 // ------------------------------------------------------------ correction WG
 template <int D>
 __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                                                const Tile& tl, const Waiter& w) {
+                                                const Tile& tl, const FwdParams& p,
+                                                const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -302,11 +343,18 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
       if (j >= tl.nkv[t]) continue;
       if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(j) & 1u, L::bPFull + t)) return;
       tc_fence_after_sync();
-      if (j > 0 && flags_s[t * 4 + wq] != 0) {
+      if (warp == 8 && lane == 0) trace_mark(p, kTrCoWake, j, t);
+      const bool flagged = j > 0 && flags_s[t * 4 + wq] != 0;
+      const float a = flagged ? alpha_s[t * kBM + r] : 1.0f;
+      // flags and alpha of step j are read: the softmax may overwrite them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bCDone + t));
+      if (flagged) {
+        // This 32-row group's reference max moved: O_t <- alpha * O_t once
+        // the previous P*V into O_t has completed, then release the group.
         if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t))
           return;
         tc_fence_after_sync();
-        const float a = alpha_s[t * kBM + r];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
@@ -318,27 +366,29 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
           tmem_st_x32(addr, x);
         }
         tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bOReady + t));
       }
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::bOReady + t));
+      if (warp == 8 && lane == 0) trace_mark(p, kTrCoArrived, j, t);
     }
   }
 }
 
 // ------------------------------------------------------------ softmax WGs
-// Column c of a 128-key block goes through the software 2^x when
-// c % PERIOD == PERIOD - 1 (PERIOD = 8: 12.5 % of the entries); PERIOD = 0
-// sends every entry through MUFU.EX2.
+// Entry pair pi (columns 2 pi, 2 pi + 1) of a 128-key block goes through the
+// software 2^x when pi % PERIOD == PERIOD - 1 (PERIOD = 8: 12.5 % of the
+// entries, PERIOD = 4: 25 %); PERIOD = 0 sends every entry through MUFU.EX2.
 template <int PERIOD>
-__host__ __device__ constexpr bool emulated_column(int c) {
+__host__ __device__ constexpr bool emulated_pair(int pi) {
   if constexpr (PERIOD <= 0) {
     return false;
   } else {
-    return (c % PERIOD) == PERIOD - 1;
+    return (pi % PERIOD) == PERIOD - 1;
   }
 }
 
-template <int D, bool CAUSAL, int EMU_PERIOD>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const Tile& tl, const FwdParams& p,
                                              const Waiter& w) {
@@ -369,6 +419,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   for (int j = 0; j < n; ++j) {
     if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(j) & 1u, L::bSFull + t))) break;
     tc_fence_after_sync();
+    const bool tracer = (wq == 0 && lane == 0);
+    if (tracer) trace_mark(p, kTrSmSReady, j, t);
     uint32_t s[128];
     tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
@@ -378,6 +430,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    if (tracer) trace_mark(p, kTrSmLoaded, j, t);
     float v[128];
 #pragma unroll
     for (int c = 0; c < 128; ++c) v[c] = __uint_as_float(s[c]);
@@ -387,21 +440,24 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       for (int c = 0; c < 128; ++c) v[c] = (c < lim) ? v[c] : -INFINITY;
     }
     // block max of the raw scores (scale > 0, so max commutes with it)
-    float mx[8];
+    float mx[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx[i] = v[i];
+    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(v[2 * i], v[2 * i + 1]);
 #pragma unroll
     for (int c = 8; c < 128; c += 8)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], v[c + i]);
-    const float m_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], v[c + 2 * i], v[c + 2 * i + 1]);
+    const float m_raw = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
     const float m_blk = m_raw * cl2;
     const float m_cand = fmaxf(m_ref, m_blk);
     // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by > tau,
     // decided for the whole warp so the correction stays warp-uniform.
     const bool need = m_cand > m_ref + p.tau;
     const bool warp_need = __any_sync(0xffffffffu, need);
+    // The correction warps must have read the flags / alpha of step j-1
+    // before they are overwritten (normally long done).
+    if (j > 0 && !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+      break;
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
       l *= alpha;
@@ -412,27 +468,37 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     if (j > 0) ++n_steps;
     if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
     const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-    // p = 2^(c*s - m_ref); part of the entries through the FMA-pipe
-    // emulation (§3.1.3), the rest through MUFU.EX2.
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
+    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the
+    // rest through MUFU.EX2. The row sum uses the fp32 p, P is stored as BF16.
+    const float2 c2 = make_float2(cl2, cl2);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
     uint32_t pk[64];
 #pragma unroll
-    for (int c = 0; c < 128; c += 2) {
-      const float x0 = fmaf(v[c], cl2, neg_m);
-      const float x1 = fmaf(v[c + 1], cl2, neg_m);
-      const bool emu0 = emulated_column<EMU_PERIOD>(c);
-      const bool emu1 = emulated_column<EMU_PERIOD>(c + 1);
-      const float p0 = emu0 ? ex2_emulated(x0) : ex2_mufu(x0);
-      const float p1 = emu1 ? ex2_emulated(x1) : ex2_mufu(x1);
-      acc[(c >> 1) & 3] += p0 + p1;
-      pk[c >> 1] = pack_bf16x2(p0, p1);
+    for (int pi = 0; pi < 64; ++pi) {
+      const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
+      const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
+                            ? ex2_emulated2(x)
+                            : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+      acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
+      pk[pi] = pack_bf16x2(pp.x, pp.y);
     }
-    l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    l += tot.x + tot.y;
+    if (tracer) trace_mark(p, kTrSmExpDone, j, t);
     tmem_st_x32(s_addr + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
     tmem_st_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
     tmem_wait_st();
     tc_fence_before_sync();
     mbar_arrive(bar(L::bPFull + t));
+    // Groups that need no rescale release O_t for the next P*V themselves;
+    // the others are released by the correction warp after rescaling.
+    __syncwarp();
+    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
+    if (tracer) trace_mark(p, kTrSmArrived, j, t);
   }
 
   // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l)
@@ -479,7 +545,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 }
 
 // ------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, int EMU_PERIOD>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
 __global__ void __launch_bounds__(kThreads, 1)
     fa4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -508,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::bSFull + t), 1);
       mbar_init(bar(L::bPFull + t), kBM);
-      mbar_init(bar(L::bOReady + t), kBM);
+      mbar_init(bar(L::bOReady + t), 4);
       mbar_init(bar(L::bPvDone + t), 1);
+      mbar_init(bar(L::bCDone + t), 4);
     }
     mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
@@ -528,11 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     regs_increase<184>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    softmax_role<D, CAUSAL, EMU_PERIOD>(warp >> 2, sbase, smem, tmem, tl, p, w);
+    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, tl, p, w);
   } else if (warp < 12) {
     regs_decrease<80>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D>(sbase, smem, tmem, tl, w);
+    correction_role<D>(sbase, smem, tmem, tl, p, w);
   } else {
     regs_decrease<64>();
     if (warp == kWarpLoad && lane == 0) {
@@ -540,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, w);
     } else if (warp == kWarpMma && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D>(sbase, tmem, tl, w);
+      mma_role<D>(sbase, tmem, tl, p, w);
     }
   }
 

@@ -69,9 +69,23 @@ typedef struct {
      * rescaled the output, [1] += number of such steps after the first key
      * block of each tile. The caller zeroes them. */
     unsigned long long *rescale_stats;
+    /* Optional DEVICE pointer to a cycle trace, or NULL (diagnostic). CTAs
+     * with block index < trace_ctas record the SM cycle counter at fixed
+     * points of the load/MMA/softmax/correction roles into
+     * trace[((cta * FA4_TRACE_EVENTS + event) * FA4_TRACE_STEPS + j) * 2 + t]
+     * for key block j < FA4_TRACE_STEPS and query tile t in {0, 1}; the
+     * buffer holds trace_ctas * FA4_TRACE_EVENTS * FA4_TRACE_STEPS * 2
+     * uint64 values. Events, in order: MMA waits for an S slot, S issued,
+     * MMA waits for the corrected O, P*V issued, softmax sees S, S in
+     * registers, P computed, P stored, correction wakes, correction done. */
+    unsigned long long *trace;
+    int trace_ctas;
 } fa4_fwd_options;
 
-/* Default options: tau = 8, exp2_emulation = 1, rescale_stats = NULL. */
+#define FA4_TRACE_EVENTS 10
+#define FA4_TRACE_STEPS 128
+
+/* Default options: tau = 8, exp2_emulation = 1, no counters, no trace. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 
 /*
@@ -111,7 +125,8 @@ fa4_status fa4_device_status(int clear, unsigned int *detail);
 
 /*
  * fa4_exp2_eval -- diagnostic: evaluate the kernel's two 2^x paths on n
- * fp32 inputs: y_emu[i] = Cody-Waite + degree-3 polynomial emulation,
+ * fp32 inputs: y_emu[i] = Cody-Waite + degree-3 polynomial emulation (the paired
+ * form the softmax runs),
  * y_mufu[i] = MUFU.EX2 (ex2.approx.ftz.f32). All three pointers are device
  * fp32 arrays of n elements (n >= 0). This is the kernel's own device
  * function ("FlashAttention-4", §3.1.3, Table 2), exported so it can be
