@@ -27,7 +27,7 @@
 // O_0 += P_0 V_j, O_1 += P_1 V_j. Because P_t aliases S_t, S_t for block
 // j+1 is only issued once O_t += P_t V_j has completed.
 //
-// Every mbarrier wait is bounded (about half a second of globaltimer). On
+// Every mbarrier wait is bounded (about half a second of SM cycles). On
 // expiry the waiting thread raises a CTA-wide abort flag and a device
 // status word; every role then leaves its loop, in-flight TMA copies and
 // MMAs are drained, and TMEM is freed before the CTA exits.
@@ -47,7 +47,8 @@ constexpr int kThreads = 512;     // 16 warps
 constexpr int kWarpLoad = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+// A wait gives up after this many SM cycles (about 0.5 s at 2 GHz).
+constexpr long long kWaitLimitCycles = 1ll << 30;
 
 enum : unsigned { kStatusTimeout = 5u };
 enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3 };
@@ -87,6 +88,11 @@ enum TraceEvent : int {
   kTrSmArrived,        // softmax: P stored, barrier arrived
   kTrCoWake,           // correction: p_full passed
   kTrCoArrived,        // correction: o_ready arrived
+  kTrMmaSGo,           // MMA: S_t dependencies met (before issuing)
+  kTrMmaPvGo,          // MMA: P_t / O_t dependencies met (before issuing)
+  kTrSmArrivedQ1,      // softmax warps 2-4 of the tile: P stored
+  kTrSmArrivedQ2,
+  kTrSmArrivedQ3,
   kTraceEvents
 };
 
@@ -135,12 +141,16 @@ struct Waiter {
 
   __device__ __forceinline__ bool slow(uint32_t bar, uint32_t parity, unsigned id,
                                        bool honour_abort) const {
-    const uint64_t t0 = globaltimer_ns();
+    // Poll first; the (cheap, SM-local) cycle counter is only read every
+    // 1024 failed polls.
+    long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
       if (mbar_try_wait(bar, parity)) return true;
-      if ((it & 63u) == 0u) {
+      if ((it & 1023u) == 0u) {
         if (honour_abort && *abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        const long long now = clock64();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > kWaitLimitCycles) {
           *abort = 1;
           if (atomicCAS(status, 0u, kStatusTimeout) == 0u) {
             status[1] = role;
@@ -279,6 +289,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
           break;
         tc_fence_after_sync();
       }
+      trace_mark(p, kTrMmaSGo, j, t);
       const uint32_t q_s = sbase + L::kQ + t * L::kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -305,6 +316,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
       if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t)))
         break;
       tc_fence_after_sync();
+      trace_mark(p, kTrMmaPvGo, j, t);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
         // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
@@ -499,6 +511,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     __syncwarp();
     if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
     if (tracer) trace_mark(p, kTrSmArrived, j, t);
+    if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t);
   }
 
   // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l)

@@ -77,12 +77,14 @@ typedef struct {
      * buffer holds trace_ctas * FA4_TRACE_EVENTS * FA4_TRACE_STEPS * 2
      * uint64 values. Events, in order: MMA waits for an S slot, S issued,
      * MMA waits for the corrected O, P*V issued, softmax sees S, S in
-     * registers, P computed, P stored, correction wakes, correction done. */
+     * registers, P computed, P stored, correction wakes, correction done,
+     * MMA S dependencies met, MMA P*V dependencies met, P stored by softmax
+     * warps 2, 3 and 4 of the tile. */
     unsigned long long *trace;
     int trace_ctas;
 } fa4_fwd_options;
 
-#define FA4_TRACE_EVENTS 10
+#define FA4_TRACE_EVENTS 15
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 1, no counters, no trace. */
