@@ -47,7 +47,7 @@ class Fa4Error(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("exp2_emulation", ctypes.c_int),
                 ("rescale_stats", ctypes.c_void_p), ("trace", ctypes.c_void_p),
-                ("trace_ctas", ctypes.c_int)]
+                ("trace_ctas", ctypes.c_int), ("strict_mma_order", ctypes.c_int)]
 
 
 TRACE_EVENTS = 15
@@ -109,7 +109,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
              tau: float = 8.0, exp2_emulation: bool = True,
              rescale_stats: Optional[torch.Tensor] = None,
-             trace: Optional[torch.Tensor] = None,
+             trace: Optional[torch.Tensor] = None, strict_mma_order: bool = False,
              stream: Optional[torch.cuda.Stream] = None) -> None:
     """Write attention forward into preallocated ``o`` and ``lse``.
 
@@ -138,6 +138,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     lib.fa4_fwd_default_options(ctypes.byref(opt))
     opt.tau = float(tau)
     opt.exp2_emulation = 1 if exp2_emulation else 0
+    opt.strict_mma_order = 1 if strict_mma_order else 0
     if rescale_stats is not None:
         if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
             raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")

@@ -123,6 +123,7 @@ void fa4_fwd_default_options(fa4_fwd_options* opt) {
   opt->rescale_stats = nullptr;
   opt->trace = nullptr;
   opt->trace_ctas = 0;
+  opt->strict_mma_order = 0;
 }
 
 const char* fa4_status_string(fa4_status s) {
@@ -154,6 +155,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (!(scale > 0.0f) || !std::isfinite(scale)) return FA4_ERR_INVALID_ARG;
   if (!std::isfinite(op.tau) || op.tau < 0.0f || op.tau > 64.0f) return FA4_ERR_INVALID_ARG;
   if (op.exp2_emulation != 0 && op.exp2_emulation != 1) return FA4_ERR_INVALID_ARG;
+  if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) return FA4_OK;  // empty output: nothing to do
   if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
@@ -220,6 +222,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.status = status;
   p.trace = op.trace;
   p.trace_ctas = op.trace ? op.trace_ctas : 0;
+  p.strict_order = op.strict_mma_order ? 1 : 0;
 
   const int emu = op.exp2_emulation ? 8 : 0;
   cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu,

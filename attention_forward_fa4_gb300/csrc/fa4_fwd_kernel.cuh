@@ -23,9 +23,9 @@
 //   P_t  (BF16, two per column) aliases the first 64 columns of S_t
 //   O_t  fp32, columns [256 + D t, 256 + D t + D)
 //
-// The MMA order per key block j is S_0, S_1 (both read K_j), then
-// O_0 += P_0 V_j, O_1 += P_1 V_j. Because P_t aliases S_t, S_t for block
-// j+1 is only issued once O_t += P_t V_j has completed.
+// The MMA thread issues the two tiles' work in ping-pong order (see
+// mma_role): each softmax WG works on its tile while the tensor core runs
+// the other tile's P*V and next S.
 //
 // Every mbarrier wait is bounded (about half a second of SM cycles). On
 // expiry the waiting thread raises a CTA-wide abort flag and a device
@@ -66,6 +66,7 @@ struct FwdParams {
   unsigned int* status;        // device status word [4]
   unsigned long long* trace;   // optional per-role cycle trace (see trace_mark)
   int trace_ctas;              // CTAs (by blockIdx.x) that record a trace
+  int strict_order;            // 1: S_t(j+1) waits for P_t(j) V_j to complete
 };
 
 // ------------------------------------------------------------ cycle trace
@@ -260,6 +261,14 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 }
 
 // ------------------------------------------------------------ MMA warp
+// Issue order (two-tile ping-pong, "FlashAttention-4" §3.1.2):
+//   S_0(0), S_1(0), then for each key block j:
+//     O_0 += P_0(j) V_j, S_0(j+1) = Q_0 K_{j+1}^T, O_1 += P_1(j) V_j, S_1(j+1)
+// so the tensor core computes tile 1's work while tile 0's softmax runs and
+// the other way round. S_t(j+1) overwrites the TMEM columns that P_t(j)
+// occupies and is issued right behind the P*V that reads them: the MMAs of
+// one issuing thread run through the SM's tensor core in issue order. With
+// FwdParams::strict_order set, S_t(j+1) instead waits for the P*V's commit.
 template <int D>
 __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Tile& tl,
                                          const FwdParams& p, const Waiter& w) {
@@ -267,48 +276,65 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major
+  constexpr uint32_t kHi = desc_hi_sw128(1024);                          // 8 rows x 128 B
   const uint32_t col_s[2] = {L::kColS0, L::kColS1};
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+  // Low descriptor halves: K-major operands (LBO unused = 16 B), V with the
+  // 64-column panel stride as LBO.
+  const uint32_t q_lo[2] = {desc_lo_sw128(sbase + L::kQ, 16),
+                            desc_lo_sw128(sbase + L::kQ + L::kTileBytes, 16)};
+  const uint32_t ring_lo_k = desc_lo_sw128(sbase + L::kRing, 16);
+  const uint32_t ring_lo_v = desc_lo_sw128(sbase + L::kRing, L::kPanelBytes);
+  constexpr uint32_t kSlotStep = L::kTileBytes >> 4;
   if (tl.nkv_max == 0) return;
+
+  auto issue_s = [&](int t, int slot) {
+    const uint32_t k_lo = ring_lo_k + slot * kSlotStep;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+      mma_ss_lohi(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(bar(L::bSFull + t));
+  };
+  auto issue_pv = [&](int t, int slot, bool first) {
+    const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
+      mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+                  kIdescPV, (!first || kk > 0) ? 1u : 0u);
+    }
+    mma_commit(bar(L::bPvDone + t));
+  };
+  auto wait_slot = [&](int idx) -> bool {
+    const int s = idx % L::kSlots;
+    const bool ok = w.wait(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u,
+                           L::bKvFull + s);
+    tc_fence_after_sync();
+    return ok;
+  };
+
   bool ok = w.wait(bar(L::bQ), 0u, L::bQ);
   tc_fence_after_sync();
-  for (int j = 0; ok && j < tl.nkv_max; ++j) {
-    // ---- S_t = Q_t K_j^T
-    const int ki = 2 * j, ks = ki % L::kSlots;
-    if (!(ok = w.wait(bar(L::bKvFull + ks), static_cast<uint32_t>(ki / L::kSlots) & 1u,
-                      L::bKvFull + ks)))
-      break;
-    tc_fence_after_sync();
-    const uint32_t k_s = sbase + L::kRing + ks * L::kTileBytes;
+  // prologue: S_0(0), S_1(0)
+  if (ok) ok = wait_slot(0);
+  if (ok) {
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (j >= tl.nkv[t]) continue;
-      trace_mark(p, kTrMmaSWait, j, t);
-      if (j > 0) {  // P_t (aliasing S_t) must be consumed before S_t is overwritten
-        if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t)))
-          break;
-        tc_fence_after_sync();
-      }
-      trace_mark(p, kTrMmaSGo, j, t);
-      const uint32_t q_s = sbase + L::kQ + t * L::kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-        mma_ss(tmem + col_s[t], smem_desc_sw128(q_s + off, 16, 1024),
-               smem_desc_sw128(k_s + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bar(L::bSFull + t));
-      trace_mark(p, kTrMmaSIssued, j, t);
+      if (tl.nkv[t] == 0) continue;
+      trace_mark(p, kTrMmaSGo, 0, t);
+      issue_s(t, 0);
+      trace_mark(p, kTrMmaSIssued, 0, t);
     }
-    if (!ok) break;
-    mma_commit(bar(L::bKvEmpty + ks));
-    // ---- O_t += P_t V_j
+    mma_commit(bar(L::bKvEmpty + 0));
+  }
+  for (int j = 0; ok && j < tl.nkv_max; ++j) {
     const int vi = 2 * j + 1, vs = vi % L::kSlots;
-    if (!(ok = w.wait(bar(L::bKvFull + vs), static_cast<uint32_t>(vi / L::kSlots) & 1u,
-                      L::bKvFull + vs)))
-      break;
-    tc_fence_after_sync();
-    const uint32_t v_s = sbase + L::kRing + vs * L::kTileBytes;
+    const int ki = 2 * j + 2, ks = ki % L::kSlots;
+    const bool next = j + 1 < tl.nkv_max;
+    if (!(ok = wait_slot(vi))) break;
+    bool k_ready = false;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (j >= tl.nkv[t]) continue;
@@ -317,18 +343,29 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
         break;
       tc_fence_after_sync();
       trace_mark(p, kTrMmaPvGo, j, t);
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
-        mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
-               smem_desc_sw128(v_s + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(bar(L::bPvDone + t));
+      issue_pv(t, vs, j == 0);
       trace_mark(p, kTrMmaPvIssued, j, t);
+      if (j + 1 >= tl.nkv[t]) continue;
+      trace_mark(p, kTrMmaSWait, j + 1, t);
+      if (!k_ready) {
+        if (!(ok = wait_slot(ki))) break;
+        k_ready = true;
+      }
+      if (p.strict_order) {
+        if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j) & 1u, L::bPvDone + t)))
+          break;
+        tc_fence_after_sync();
+      }
+      trace_mark(p, kTrMmaSGo, j + 1, t);
+      issue_s(t, ks);
+      trace_mark(p, kTrMmaSIssued, j + 1, t);
     }
     if (!ok) break;
     mma_commit(bar(L::bKvEmpty + vs));
+    if (next) {
+      // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
+      mma_commit(bar(L::bKvEmpty + ks));
+    }
   }
   // Every MMA issued above has completed once this commit arrives.
   mma_commit(bar(L::bDrain));
@@ -367,15 +404,15 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t))
           return;
         tc_fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t x[16];
+          const uint32_t addr = lane_base + col_o[t] + c * 16;
+          tmem_ld_x16(addr, x);
+          tmem_wait_ld_x16(x);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t x[32];
-          const uint32_t addr = lane_base + col_o[t] + c * 32;
-          tmem_ld_x32(addr, x);
-          tmem_wait_ld_x32(x);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * a);
-          tmem_st_x32(addr, x);
+          for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * a);
+          tmem_st_x16(addr, x);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -605,16 +642,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Register split: 256 softmax threads x 176 + 128 correction x 72 +
+  // 128 load/MMA x 88 = 65,536 = 512 threads x 128 at launch.
   if (warp < 8) {
-    regs_increase<184>();
+    regs_increase<176>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
     softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, tl, p, w);
   } else if (warp < 12) {
-    regs_decrease<80>();
+    regs_decrease<72>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
     correction_role<D>(sbase, smem, tmem, tl, p, w);
   } else {
-    regs_decrease<64>();
+    regs_decrease<88>();
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
       load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, w);

@@ -82,12 +82,21 @@ typedef struct {
      * warps 2, 3 and 4 of the tile. */
     unsigned long long *trace;
     int trace_ctas;
+    /* 0 (default): the MMA that computes the next score tile S_t into the
+     * tensor-memory columns where the probabilities P_t of the previous
+     * key block live is issued right behind the P_t*V MMA that reads them,
+     * relying on the tensor core running one thread's MMAs in issue order
+     * (the two-tile ping-pong of "FlashAttention-4" §3.1.2). 1: wait for
+     * the P_t*V MMA to complete first (slower; the PTX memory model only
+     * promises issue order for MMAs into the same accumulator). */
+    int strict_mma_order;
 } fa4_fwd_options;
 
 #define FA4_TRACE_EVENTS 15
 #define FA4_TRACE_STEPS 128
 
-/* Default options: tau = 8, exp2_emulation = 1, no counters, no trace. */
+/* Default options: tau = 8, exp2_emulation = 1, no counters, no trace,
+ * strict_mma_order = 0. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 
 /*

@@ -179,3 +179,19 @@ def test_exp2_emulation_table2_on_device():
     ints = torch.arange(-126, 9, dtype=torch.float32)
     yi, _ = fa4.exp2_eval(ints.to(DEV))
     assert torch.equal(yi.cpu(), torch.exp2(ints))
+
+
+# ------------------------------------------------------------ MMA issue order
+@pytest.mark.parametrize("shape", [(2, 16, 16, 2048, 2048, 128, True),
+                                   (1, 8, 2, 1536, 1536, 128, False),
+                                   (4, 8, 8, 1024, 1024, 64, True)])
+def test_back_to_back_issue_equals_strict_order(shape):
+    """The next S MMA is issued right behind the P*V MMA that reads the same
+    tensor-memory columns; waiting for the P*V first must give bit-identical
+    output (repeated, to catch a rare reordering)."""
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=41, dist="wide")
+    o_s, l_s = _run(q, k, v, causal, strict_mma_order=True)
+    for _ in range(5):
+        o_f, l_f = _run(q, k, v, causal)
+        assert torch.equal(o_f, o_s) and torch.equal(l_f, l_s)
