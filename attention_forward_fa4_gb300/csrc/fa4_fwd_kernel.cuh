@@ -437,32 +437,6 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
-// One 32-key chunk (columns 32 CHUNK .. 32 CHUNK + 31) of a row:
-// p = 2^(c * s - m) for its scores (c2 = (c, c), nm2 = (-m, -m)) on pairs of
-// entries with FFMA2 / FADD2; one pair in EMU_PAIR_PERIOD goes through the
-// FMA-pipe emulation (§3.1.3), the rest through MUFU.EX2. Keys at or past
-// column `lim` count as -inf when `masked`. Folds the raw scores into the
-// running max mx, adds p (fp32) to the running sums acc and packs p to
-// BF16 pairs in pk[0..15].
-template <int EMU_PAIR_PERIOD, int CHUNK>
-__device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], bool masked, int lim, float2 c2,
-                                          float2 nm2, float (&mx)[4], float2 (&acc)[4],
-                                          uint32_t* pk) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int c0 = CHUNK * 32 + 2 * i;
-    const float a = (!masked || c0 < lim) ? __uint_as_float(s[2 * i]) : -INFINITY;
-    const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(s[2 * i + 1]) : -INFINITY;
-    mx[i & 3] = fmax3(mx[i & 3], a, b);
-    const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
-    const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(CHUNK * 16 + i)
-                          ? ex2_emulated2(x)
-                          : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-    acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-    pk[i] = pack_bf16x2(pp.x, pp.y);
-  }
-}
-
 template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const Tile& tl, const FwdParams& p,
@@ -496,98 +470,71 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tc_fence_after_sync();
     const bool tracer = (wq == 0 && lane == 0);
     if (tracer) trace_mark(p, kTrSmSReady, j, t);
-    const bool masked = (j + 1) * kBN > lim_min;     // tile-uniform: some keys masked
-    const int lim = lim_row - j * kBN;                 // this row's first masked column
-    const float2 c2 = make_float2(cl2, cl2);
-    float2 acc[4];
-    float mx[4];
-    uint32_t pk[64];
-    // Speculative pass: while every row of the warp has a reference max and
-    // tau > 0, exponentiate against the current m~ chunk by chunk as the
-    // scores arrive from TMEM; the block max is folded in alongside. If no
-    // row of the warp moves past m~ + tau (the usual case) these are exactly
-    // the probabilities of the conditional rescale; otherwise the row is
-    // reloaded (S is still intact in TMEM) and redone below.
-    const bool spec = p.tau > 0.0f && __all_sync(0xffffffffu, m_ref != -INFINITY);
-    bool warp_need = false;
-    float m_cand = m_ref;
-    if (spec) {
-      const float2 nm2 = make_float2(-m_ref, -m_ref);
+    uint32_t s[128];
+    tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    if (tracer) trace_mark(p, kTrSmLoaded, j, t);
+    float v[128];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i] = make_float2(0.0f, 0.0f);
-        mx[i] = -INFINITY;
-      }
-      uint32_t sa[32], sb[32];
-      tmem_ld_x32(s_addr + 0, sa);
-      tmem_wait_ld_x32(sa);
-      tmem_ld_x32(s_addr + 32, sb);
-      if (tracer) trace_mark(p, kTrSmLoaded, j, t);
-      exp_chunk<EMU_PAIR_PERIOD, 0>(sa, masked, lim, c2, nm2, mx, acc, &pk[0]);
-      tmem_wait_ld_x32(sb);
-      tmem_ld_x32(s_addr + 64, sa);
-      exp_chunk<EMU_PAIR_PERIOD, 1>(sb, masked, lim, c2, nm2, mx, acc, &pk[16]);
-      tmem_wait_ld_x32(sa);
-      tmem_ld_x32(s_addr + 96, sb);
-      exp_chunk<EMU_PAIR_PERIOD, 2>(sa, masked, lim, c2, nm2, mx, acc, &pk[32]);
-      tmem_wait_ld_x32(sb);
-      exp_chunk<EMU_PAIR_PERIOD, 3>(sb, masked, lim, c2, nm2, mx, acc, &pk[48]);
-      const float m_blk = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2;
-      m_cand = fmaxf(m_ref, m_blk);
-      warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
+    for (int c = 0; c < 128; ++c) v[c] = __uint_as_float(s[c]);
+    if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
+      const int lim = lim_row - j * kBN;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) v[c] = (c < lim) ? v[c] : -INFINITY;
     }
+    // block max of the raw scores (scale > 0, so max commutes with it)
+    float mx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int c = 8; c < 128; c += 8)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], v[c + 2 * i], v[c + 2 * i + 1]);
+    const float m_raw = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+    const float m_blk = m_raw * cl2;
+    const float m_cand = fmaxf(m_ref, m_blk);
+    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by > tau,
+    // decided for the whole warp so the correction stays warp-uniform.
+    const bool need = m_cand > m_ref + p.tau;
+    const bool warp_need = __any_sync(0xffffffffu, need);
     // The correction warps must have read the flags / alpha of step j-1
     // before they are overwritten (normally long done).
     if (j > 0 && !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
       break;
-    if (!spec || warp_need) {
-      // Full-row path: first block, tau = 0, or a row group whose max moved.
-      uint32_t sr[128];
-      tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      if (!spec) {
-        if (tracer) trace_mark(p, kTrSmLoaded, j, t);
-        // block max of the raw scores (scale > 0, so max commutes with it)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c0 = c + 2 * i;
-            const float a = (!masked || c0 < lim) ? __uint_as_float(sr[c0]) : -INFINITY;
-            const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(sr[c0 + 1]) : -INFINITY;
-            mx[i] = fmax3(mx[i], a, b);
-          }
-        m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
-        // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by
-        // more than tau, decided per warp so the correction stays uniform.
-        warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-      }
-      if (warp_need) {
-        const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
-        l *= alpha;
-        if (m_cand != -INFINITY) m_ref = m_cand;
-        alpha_s[t * kBM + r] = alpha;
-        if (j > 0) ++n_rescaled;
-      }
-      const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-      const float2 nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      exp_chunk<EMU_PAIR_PERIOD, 0>(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]), masked, lim, c2, nm2, mx, acc, &pk[0]);
-      exp_chunk<EMU_PAIR_PERIOD, 1>(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]), masked, lim, c2, nm2, mx, acc, &pk[16]);
-      exp_chunk<EMU_PAIR_PERIOD, 2>(*reinterpret_cast<uint32_t(*)[32]>(&sr[64]), masked, lim, c2, nm2, mx, acc, &pk[32]);
-      exp_chunk<EMU_PAIR_PERIOD, 3>(*reinterpret_cast<uint32_t(*)[32]>(&sr[96]), masked, lim, c2, nm2, mx, acc, &pk[48]);
+    if (warp_need) {
+      const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+      l *= alpha;
+      if (m_cand != -INFINITY) m_ref = m_cand;
+      alpha_s[t * kBM + r] = alpha;
+      if (j > 0) ++n_rescaled;
     }
     if (j > 0) ++n_steps;
     if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+    const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+    // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
+    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the
+    // rest through MUFU.EX2. The row sum uses the fp32 p, P is stored as BF16.
+    const float2 c2 = make_float2(cl2, cl2);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    uint32_t pk[64];
+#pragma unroll
+    for (int pi = 0; pi < 64; ++pi) {
+      const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
+      const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
+                            ? ex2_emulated2(x)
+                            : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+      acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
+      pk[pi] = pack_bf16x2(pp.x, pp.y);
+    }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
     if (tracer) trace_mark(p, kTrSmExpDone, j, t);
