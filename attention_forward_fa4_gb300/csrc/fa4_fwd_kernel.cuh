@@ -94,6 +94,7 @@ enum TraceEvent : int {
   kTrSmArrivedQ1,      // softmax warps 2-4 of the tile: P stored
   kTrSmArrivedQ2,
   kTrSmArrivedQ3,
+  kTrSmMaxDone,        // softmax: block max known, rescale decided
   kTraceEvents
 };
 
@@ -123,7 +124,8 @@ struct Smem {
   static constexpr int bOReady = bPFull + 2;             // [2]
   static constexpr int bPvDone = bOReady + 2;            // [2]
   static constexpr int bCDone = bPvDone + 2;             // [2]
-  static constexpr int bDrain = bCDone + 2;
+  static constexpr int bPHalf = bCDone + 2;              // [2 tiles][2 halves]
+  static constexpr int bDrain = bPHalf + 4;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
   static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
@@ -297,15 +299,25 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
     }
     mma_commit(bar(L::bSFull + t));
   };
-  auto issue_pv = [&](int t, int slot, bool first) {
+  // O_t += P_t V_j in two halves of 64 keys; the second half waits for the
+  // softmax warps to have stored the second half of P. Returns false on abort.
+  auto issue_pv = [&](int t, int slot, int j) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
-      // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
-      mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
-                  kIdescPV, (!first || kk > 0) ? 1u : 0u);
+    for (int half = 0; half < 2; ++half) {
+      if (!w.wait(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(j) & 1u, L::bPHalf + 2 * t + half))
+        return false;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < kBN / 32; ++k) {
+        // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
+        const int kk = half * (kBN / 32) + k;
+        mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+                    kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      }
     }
     mma_commit(bar(L::bPvDone + t));
+    return true;
   };
   auto wait_slot = [&](int idx) -> bool {
     const int s = idx % L::kSlots;
@@ -343,7 +355,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
         break;
       tc_fence_after_sync();
       trace_mark(p, kTrMmaPvGo, j, t);
-      issue_pv(t, vs, j == 0);
+      if (!(ok = issue_pv(t, vs, j))) break;
       trace_mark(p, kTrMmaPvIssued, j, t);
       if (j + 1 >= tl.nkv[t]) continue;
       trace_mark(p, kTrMmaSWait, j + 1, t);
@@ -475,6 +487,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    // The correction warps must have read the flags / alpha of step j-1
+    // before they are overwritten (normally long done); checked while the
+    // scores are in flight from TMEM.
+    if (j > 0 && !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+      break;
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
@@ -503,10 +520,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // decided for the whole warp so the correction stays warp-uniform.
     const bool need = m_cand > m_ref + p.tau;
     const bool warp_need = __any_sync(0xffffffffu, need);
-    // The correction warps must have read the flags / alpha of step j-1
-    // before they are overwritten (normally long done).
-    if (j > 0 && !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
-      break;
+    if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
       l *= alpha;
@@ -516,37 +530,46 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     }
     if (j > 0) ++n_steps;
     if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+    // Decision made: the correction warps may read flag / alpha and rescale
+    // O_t while the exponentials below run; row groups that need no rescale
+    // release O_t for the next P*V right away.
+    mbar_arrive(bar(L::bPFull + t));
+    __syncwarp();
+    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
     const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
     // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
     // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the
-    // rest through MUFU.EX2. The row sum uses the fp32 p, P is stored as BF16.
+    // rest through MUFU.EX2. The row sum uses the fp32 p, P is stored as BF16
+    // in two halves (keys 0-63, 64-127), each released to the MMA warp as
+    // soon as it is in TMEM so the first half of P*V overlaps the second
+    // half of the exponentials.
     const float2 c2 = make_float2(cl2, cl2);
     const float2 nm2 = make_float2(neg_m, neg_m);
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    uint32_t pk[64];
 #pragma unroll
-    for (int pi = 0; pi < 64; ++pi) {
-      const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
-      const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
-                            ? ex2_emulated2(x)
-                            : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-      acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
-      pk[pi] = pack_bf16x2(pp.x, pp.y);
+    for (int half = 0; half < 2; ++half) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int pi = half * 32 + i;
+        const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
+        const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
+                              ? ex2_emulated2(x)
+                              : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+        acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+        pk[i] = pack_bf16x2(pp.x, pp.y);
+      }
+      tmem_st_x32(s_addr + half * 32, pk);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t + half));
     }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
     if (tracer) trace_mark(p, kTrSmExpDone, j, t);
-    tmem_st_x32(s_addr + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-    tmem_st_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-    tmem_wait_st();
-    tc_fence_before_sync();
-    mbar_arrive(bar(L::bPFull + t));
-    // Groups that need no rescale release O_t for the next P*V themselves;
-    // the others are released by the correction warp after rescaling.
-    __syncwarp();
-    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
     if (tracer) trace_mark(p, kTrSmArrived, j, t);
     if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t);
   }
@@ -627,6 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bOReady + t), 4);
       mbar_init(bar(L::bPvDone + t), 1);
       mbar_init(bar(L::bCDone + t), 4);
+      mbar_init(bar(L::bPHalf + 2 * t), 4);
+      mbar_init(bar(L::bPHalf + 2 * t + 1), 4);
     }
     mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
