@@ -39,6 +39,25 @@
 #include "fa4_exp2.cuh"
 #include "fa4_ptx.cuh"
 
+// Tunables (compile-time):
+//   FA4_P_SLICES     1: P is stored and released to P*V as one 128-key block;
+//                    2: in two 64-key halves so P*V starts on the first half
+//                    while the second is being exponentiated.
+//   FA4_CDONE_EARLY  1: the softmax checks that the correction warps read the
+//                    previous flags while its scores load from TMEM; 0: after
+//                    the block max.
+//   FA4_WAIT_SPIN    1: waits poll with mbarrier.test_wait (no suspension);
+//                    0: mbarrier.try_wait (the thread may be suspended).
+#ifndef FA4_P_SLICES
+#define FA4_P_SLICES 1
+#endif
+#ifndef FA4_CDONE_EARLY
+#define FA4_CDONE_EARLY 0
+#endif
+#ifndef FA4_WAIT_SPIN
+#define FA4_WAIT_SPIN 0
+#endif
+
 namespace fa4 {
 
 constexpr int kBM = 128;          // query rows per tile = TMEM lanes
@@ -148,7 +167,7 @@ struct Waiter {
     // 1024 failed polls.
     long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(bar, parity)) return true;
+      if (FA4_WAIT_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
       if ((it & 1023u) == 0u) {
         if (honour_abort && *abort) return false;
         const long long now = clock64();
@@ -304,14 +323,14 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
   auto issue_pv = [&](int t, int slot, int j) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < FA4_P_SLICES; ++half) {
       if (!w.wait(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(j) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
 #pragma unroll
-      for (int k = 0; k < kBN / 32; ++k) {
+      for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
         // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
-        const int kk = half * (kBN / 32) + k;
+        const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
         mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
                     kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
@@ -488,9 +507,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     // The correction warps must have read the flags / alpha of step j-1
-    // before they are overwritten (normally long done); checked while the
-    // scores are in flight from TMEM.
-    if (j > 0 && !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+    // before they are overwritten (normally long done).
+    if (FA4_CDONE_EARLY && j > 0 &&
+        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
       break;
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
@@ -520,6 +539,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // decided for the whole warp so the correction stays warp-uniform.
     const bool need = m_cand > m_ref + p.tau;
     const bool warp_need = __any_sync(0xffffffffu, need);
+    if (!FA4_CDONE_EARLY && j > 0 &&
+        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+      break;
     if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
@@ -548,12 +570,13 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t pk[32];
+    for (int half = 0; half < FA4_P_SLICES; ++half) {
+      uint32_t pk[kSliceCols];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int pi = half * 32 + i;
+      for (int i = 0; i < kSliceCols; ++i) {
+        const int pi = half * kSliceCols + i;
         const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
         const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
                               ? ex2_emulated2(x)
@@ -561,7 +584,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
         acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
         pk[i] = pack_bf16x2(pp.x, pp.y);
       }
-      tmem_st_x32(s_addr + half * 32, pk);
+#pragma unroll
+      for (int q = 0; q < kSliceCols / 32; ++q)
+        tmem_st_x32(s_addr + half * kSliceCols + q * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[q * 32]));
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
