@@ -57,6 +57,13 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
+//   FA4_SPEC_EXP     1: once a 32-row group has a reference max, exponentiate
+//                    against it in the same pass that finds the block max;
+//                    redo the pass (S reloaded from TMEM) only when the group
+//                    rescales. 0: block max first, then exponentiate.
+#ifndef FA4_SPEC_EXP
+#define FA4_SPEC_EXP 0
+#endif
 
 namespace fa4 {
 
@@ -516,77 +523,118 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     if (tracer) trace_mark(p, kTrSmLoaded, j, t);
-    float v[128];
+    const bool masked = (j + 1) * kBN > lim_min;     // tile-uniform: some keys masked
+    const int lim = lim_row - j * kBN;                 // this row's first masked column
+    // Speculate only when every row of the warp has a reference max.
+    const bool spec = FA4_SPEC_EXP && p.tau > 0.0f && __all_sync(0xffffffffu, m_ref != -INFINITY);
+    bool warp_need = false;
+    float m_cand = m_ref;
+    if (!spec) {
+      // block max of the raw scores (scale > 0, so max commutes with it)
+      float mx[4];
 #pragma unroll
-    for (int c = 0; c < 128; ++c) v[c] = __uint_as_float(s[c]);
-    if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
-      const int lim = lim_row - j * kBN;
+      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) v[c] = (c < lim) ? v[c] : -INFINITY;
+      for (int c = 0; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c0 = c + 2 * i;
+          const float a = (!masked || c0 < lim) ? __uint_as_float(s[c0]) : -INFINITY;
+          const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(s[c0 + 1]) : -INFINITY;
+          mx[i] = fmax3(mx[i], a, b);
+        }
+      m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
+      // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
+      // than tau, decided per warp so the correction stays warp-uniform.
+      warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
     }
-    // block max of the raw scores (scale > 0, so max commutes with it)
-    float mx[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-    for (int c = 8; c < 128; c += 8)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], v[c + 2 * i], v[c + 2 * i + 1]);
-    const float m_raw = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-    const float m_blk = m_raw * cl2;
-    const float m_cand = fmaxf(m_ref, m_blk);
-    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by > tau,
-    // decided for the whole warp so the correction stays warp-uniform.
-    const bool need = m_cand > m_ref + p.tau;
-    const bool warp_need = __any_sync(0xffffffffu, need);
-    if (!FA4_CDONE_EARLY && j > 0 &&
-        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
-      break;
-    if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
-    if (warp_need) {
-      const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
-      l *= alpha;
-      if (m_cand != -INFINITY) m_ref = m_cand;
-      alpha_s[t * kBM + r] = alpha;
-      if (j > 0) ++n_rescaled;
+    if (!spec) {
+      if (!FA4_CDONE_EARLY && j > 0 &&
+          !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+        break;
+      if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
+      if (warp_need) {
+        const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+        l *= alpha;
+        if (m_cand != -INFINITY) m_ref = m_cand;
+        alpha_s[t * kBM + r] = alpha;
+        if (j > 0) ++n_rescaled;
+      }
+      if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+      // Decision made: the correction warps may read flag / alpha and
+      // rescale O_t while the exponentials run; row groups that need no
+      // rescale release O_t for the next P*V right away.
+      mbar_arrive(bar(L::bPFull + t));
+      __syncwarp();
+      if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
     }
     if (j > 0) ++n_steps;
-    if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
-    // Decision made: the correction warps may read flag / alpha and rescale
-    // O_t while the exponentials below run; row groups that need no rescale
-    // release O_t for the next P*V right away.
-    mbar_arrive(bar(L::bPFull + t));
-    __syncwarp();
-    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
-    const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
     // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
-    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the
-    // rest through MUFU.EX2. The row sum uses the fp32 p, P is stored as BF16
-    // in two halves (keys 0-63, 64-127), each released to the MMA warp as
-    // soon as it is in TMEM so the first half of P*V overlaps the second
-    // half of the exponentials.
+    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the rest
+    // through MUFU.EX2. The row sum uses the fp32 p; P is stored as BF16.
     const float2 c2 = make_float2(cl2, cl2);
-    const float2 nm2 = make_float2(neg_m, neg_m);
     float2 acc[4];
+    uint32_t pk[64];
+    for (int pass = 0;; ++pass) {
+      const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      float mx[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
+      for (int i = 0; i < 4; ++i) {
+        acc[i] = make_float2(0.0f, 0.0f);
+        mx[i] = -INFINITY;
+      }
 #pragma unroll
-    for (int half = 0; half < FA4_P_SLICES; ++half) {
-      uint32_t pk[kSliceCols];
-#pragma unroll
-      for (int i = 0; i < kSliceCols; ++i) {
-        const int pi = half * kSliceCols + i;
-        const float2 x = __ffma2_rn(make_float2(v[2 * pi], v[2 * pi + 1]), c2, nm2);
+      for (int pi = 0; pi < 64; ++pi) {
+        const int c0 = 2 * pi;
+        const float a = (!masked || c0 < lim) ? __uint_as_float(s[c0]) : -INFINITY;
+        const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(s[c0 + 1]) : -INFINITY;
+        if (spec && pass == 0) mx[pi & 3] = fmax3(mx[pi & 3], a, b);
+        const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
         const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
                               ? ex2_emulated2(x)
                               : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-        acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-        pk[i] = pack_bf16x2(pp.x, pp.y);
+        acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
+        pk[pi] = pack_bf16x2(pp.x, pp.y);
       }
+      if (!spec || pass > 0) break;
+      // Speculative pass done: does any row of the warp move past m~ + tau?
+      m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
+      warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
+      if (j > 0 &&
+          !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+        break;
+      if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
+      if (warp_need) {
+        const float alpha = ex2_mufu(m_ref - m_cand);
+        l *= alpha;
+        m_ref = m_cand;
+        alpha_s[t * kBM + r] = alpha;
+        if (j > 0) ++n_rescaled;
+      }
+      if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+      mbar_arrive(bar(L::bPFull + t));
+      __syncwarp();
+      if (lane == 0 && !warp_need) mbar_arrive(bar(L::bOReady + t));
+      if (!warp_need) break;
+      // The scores are still intact in TMEM (P is not stored yet): reload.
+      tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    }
+    if (!ok) break;
+    constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
+#pragma unroll
+    for (int half = 0; half < FA4_P_SLICES; ++half) {
 #pragma unroll
       for (int q = 0; q < kSliceCols / 32; ++q)
-        tmem_st_x32(s_addr + half * kSliceCols + q * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[q * 32]));
+        tmem_st_x32(s_addr + half * kSliceCols + q * 32,
+                    *reinterpret_cast<const uint32_t(*)[32]>(&pk[half * kSliceCols + q * 32]));
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
