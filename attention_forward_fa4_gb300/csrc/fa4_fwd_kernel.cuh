@@ -523,8 +523,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     if (tracer) trace_mark(p, kTrSmLoaded, j, t);
-    const bool masked = (j + 1) * kBN > lim_min;     // tile-uniform: some keys masked
-    const int lim = lim_row - j * kBN;                 // this row's first masked column
+    if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
+      const int lim = lim_row - j * kBN;                 // this row's first masked column
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
+    }
     // Speculate only when every row of the warp has a reference max.
     const bool spec = FA4_SPEC_EXP && p.tau > 0.0f && __all_sync(0xffffffffu, m_ref != -INFINITY);
     bool warp_need = false;
@@ -533,16 +536,12 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       // block max of the raw scores (scale > 0, so max commutes with it)
       float mx[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+      for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
-      for (int c = 0; c < 128; c += 8)
+      for (int c = 8; c < 128; c += 8)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c0 = c + 2 * i;
-          const float a = (!masked || c0 < lim) ? __uint_as_float(s[c0]) : -INFINITY;
-          const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(s[c0 + 1]) : -INFINITY;
-          mx[i] = fmax3(mx[i], a, b);
-        }
+        for (int i = 0; i < 4; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
       m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
       // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
       // than tau, decided per warp so the correction stays warp-uniform.
@@ -586,9 +585,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       }
 #pragma unroll
       for (int pi = 0; pi < 64; ++pi) {
-        const int c0 = 2 * pi;
-        const float a = (!masked || c0 < lim) ? __uint_as_float(s[c0]) : -INFINITY;
-        const float b = (!masked || c0 + 1 < lim) ? __uint_as_float(s[c0 + 1]) : -INFINITY;
+        const float a = __uint_as_float(s[2 * pi]);
+        const float b = __uint_as_float(s[2 * pi + 1]);
         if (spec && pass == 0) mx[pi & 3] = fmax3(mx[pi & 3], a, b);
         const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
         const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
@@ -626,6 +624,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
       tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
       tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      if ((j + 1) * kBN > lim_min) {
+        const int lim = lim_row - j * kBN;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
+      }
     }
     if (!ok) break;
     constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
