@@ -57,13 +57,7 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
-//   FA4_SPEC_EXP     1: once a 32-row group has a reference max, exponentiate
-//                    against it in the same pass that finds the block max;
-//                    redo the pass (S reloaded from TMEM) only when the group
-//                    rescales. 0: block max first, then exponentiate.
-#ifndef FA4_SPEC_EXP
-#define FA4_SPEC_EXP 0
-#endif
+
 
 namespace fa4 {
 
@@ -121,6 +115,9 @@ enum TraceEvent : int {
   kTrSmArrivedQ2,
   kTrSmArrivedQ3,
   kTrSmMaxDone,        // softmax: block max known, rescale decided
+  kTrMmaCommitted,     // MMA: slot-release commits of key block j issued
+  kTrMmaVReady,        // MMA: V_j in shared memory (before any P_t V_j)
+  kTrLoadIssued,       // load warp: V_j copy issued (t = 0) / K_j copy issued (t = 1)
   kTraceEvents
 };
 
@@ -252,7 +249,7 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p) {
 template <int D>
 __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, uint32_t sbase,
-                                          const Tile& tl, const Waiter& w) {
+                                          const Tile& tl, const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   if (tl.nkv_max == 0) return;
@@ -277,6 +274,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
       tma_load_4d(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm, bar(L::bKvFull + s),
                   pn * 64, tl.hk, row, tl.b);
     issued = idx + 1;
+    trace_mark(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1);
   }
   if (issued < total || *w.abort) {
     // Let every copy this warp started land before the CTA frees its memory.
@@ -372,6 +370,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
     const int ki = 2 * j + 2, ks = ki % L::kSlots;
     const bool next = j + 1 < tl.nkv_max;
     if (!(ok = wait_slot(vi))) break;
+    trace_mark(p, kTrMmaVReady, j, 0);
     bool k_ready = false;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -404,6 +403,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
       // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
       mma_commit(bar(L::bKvEmpty + ks));
     }
+    trace_mark(p, kTrMmaCommitted, j, 0);
   }
   // Every MMA issued above has completed once this commit arrives.
   mma_commit(bar(L::bDrain));
@@ -528,109 +528,58 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
     }
-    // Speculate only when every row of the warp has a reference max.
-    const bool spec = FA4_SPEC_EXP && p.tau > 0.0f && __all_sync(0xffffffffu, m_ref != -INFINITY);
-    bool warp_need = false;
-    float m_cand = m_ref;
-    if (!spec) {
-      // block max of the raw scores (scale > 0, so max commutes with it)
-      float mx[4];
+    // block max of the raw scores (scale > 0, so max commutes with it)
+    float mx[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+    for (int c = 8; c < 128; c += 8)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-      m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
-      // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
-      // than tau, decided per warp so the correction stays warp-uniform.
-      warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
+      for (int i = 0; i < 4; ++i)
+        mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+    const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
+    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
+    // than tau, decided per warp so the correction stays warp-uniform.
+    const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
+    if (!FA4_CDONE_EARLY && j > 0 &&
+        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+      break;
+    if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
+    if (warp_need) {
+      const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+      l *= alpha;
+      if (m_cand != -INFINITY) m_ref = m_cand;
+      alpha_s[t * kBM + r] = alpha;
+      if (j > 0) ++n_rescaled;
     }
-    if (!spec) {
-      if (!FA4_CDONE_EARLY && j > 0 &&
-          !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
-        break;
-      if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
-      if (warp_need) {
-        const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
-        l *= alpha;
-        if (m_cand != -INFINITY) m_ref = m_cand;
-        alpha_s[t * kBM + r] = alpha;
-        if (j > 0) ++n_rescaled;
-      }
-      if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
-      // Decision made: the correction warps may read flag / alpha and
-      // rescale O_t while the exponentials run; row groups that need no
-      // rescale release O_t for the next P*V right away.
-      mbar_arrive(bar(L::bPFull + t));
-      __syncwarp();
-      if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
-    }
+    if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+    // Decision made: the correction warps may read flag / alpha and rescale
+    // O_t while the exponentials run; row groups that need no rescale
+    // release O_t for the next P*V right away.
+    mbar_arrive(bar(L::bPFull + t));
+    __syncwarp();
+    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
     if (j > 0) ++n_steps;
     // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
     // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the rest
     // through MUFU.EX2. The row sum uses the fp32 p; P is stored as BF16.
+    const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
     const float2 c2 = make_float2(cl2, cl2);
+    const float2 nm2 = make_float2(neg_m, neg_m);
     float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
     uint32_t pk[64];
-    for (int pass = 0;; ++pass) {
-      const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-      const float2 nm2 = make_float2(neg_m, neg_m);
-      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i] = make_float2(0.0f, 0.0f);
-        mx[i] = -INFINITY;
-      }
-#pragma unroll
-      for (int pi = 0; pi < 64; ++pi) {
-        const float a = __uint_as_float(s[2 * pi]);
-        const float b = __uint_as_float(s[2 * pi + 1]);
-        if (spec && pass == 0) mx[pi & 3] = fmax3(mx[pi & 3], a, b);
-        const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
-        const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
-                              ? ex2_emulated2(x)
-                              : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-        acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
-        pk[pi] = pack_bf16x2(pp.x, pp.y);
-      }
-      if (!spec || pass > 0) break;
-      // Speculative pass done: does any row of the warp move past m~ + tau?
-      m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
-      warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-      if (j > 0 &&
-          !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
-        break;
-      if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
-      if (warp_need) {
-        const float alpha = ex2_mufu(m_ref - m_cand);
-        l *= alpha;
-        m_ref = m_cand;
-        alpha_s[t * kBM + r] = alpha;
-        if (j > 0) ++n_rescaled;
-      }
-      if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
-      mbar_arrive(bar(L::bPFull + t));
-      __syncwarp();
-      if (lane == 0 && !warp_need) mbar_arrive(bar(L::bOReady + t));
-      if (!warp_need) break;
-      // The scores are still intact in TMEM (P is not stored yet): reload.
-      tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      if ((j + 1) * kBN > lim_min) {
-        const int lim = lim_row - j * kBN;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
-      }
+    for (int pi = 0; pi < 64; ++pi) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * pi]), __uint_as_float(s[2 * pi + 1])),
+                                  c2, nm2);
+      const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
+                            ? ex2_emulated2(x)
+                            : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+      acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
+      pk[pi] = pack_bf16x2(pp.x, pp.y);
     }
-    if (!ok) break;
     constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
@@ -757,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<88>();
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, w);
+      load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, p, w);
     } else if (warp == kWarpMma && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleMma};
       mma_role<D>(sbase, tmem, tl, p, w);

@@ -79,7 +79,9 @@ typedef struct {
      * MMA waits for the corrected O, P*V issued, softmax sees S, S in
      * registers, P computed, P stored, correction wakes, correction done,
      * MMA S dependencies met, MMA P*V dependencies met, P stored by softmax
-     * warps 2, 3 and 4 of the tile, softmax block max known. */
+     * warps 2, 3 and 4 of the tile, softmax block max known, MMA released
+     * the key block's slots (t = 0), V_j resident (t = 0), load warp issued
+     * V_j (t = 0) / K_j (t = 1). */
     unsigned long long *trace;
     int trace_ctas;
     /* 0 (default): the MMA that computes the next score tile S_t into the
@@ -92,7 +94,7 @@ typedef struct {
     int strict_mma_order;
 } fa4_fwd_options;
 
-#define FA4_TRACE_EVENTS 16
+#define FA4_TRACE_EVENTS 19
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 1, no counters, no trace,
