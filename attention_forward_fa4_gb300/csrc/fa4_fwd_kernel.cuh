@@ -15,9 +15,8 @@
 //               that need no rescale never wait for it
 
 //   warp 12     TMA load warp: Q once, then K_j / V_j into a ring of slots
-//   warps 13-14 MMA warps: one thread each issues the tcgen05.mma of one
-//               query tile
-//   warp 15     idle
+//   warp 13     MMA warp: one thread issues every tcgen05.mma
+//   warps 14-15 idle
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_t  = Q_t K_j^T   fp32, columns [128 t, 128 t + 128)
@@ -142,15 +141,15 @@ struct Smem {
   // barrier ids
   static constexpr int bQ = 0;
   static constexpr int bKvFull = 1;
-  static constexpr int bKvEmpty = bKvFull + kSlots;      // [2 tiles][kSlots]
-  static constexpr int bSFull = bKvEmpty + 2 * kSlots;   // [2]
+  static constexpr int bKvEmpty = bKvFull + kSlots;
+  static constexpr int bSFull = bKvEmpty + kSlots;       // [2]
   static constexpr int bPFull = bSFull + 2;              // [2]
   static constexpr int bOReady = bPFull + 2;             // [2]
   static constexpr int bPvDone = bOReady + 2;            // [2]
   static constexpr int bCDone = bPvDone + 2;             // [2]
   static constexpr int bPHalf = bCDone + 2;              // [2 tiles][2 halves]
-  static constexpr int bDrain = bPHalf + 4;              // [2]
-  static constexpr int kNumBars = bDrain + 2;
+  static constexpr int bDrain = bPHalf + 4;
+  static constexpr int kNumBars = bDrain + 1;
   static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
   static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
   static constexpr int kMisc = kFlags + 8 * 4;           // tmem base, abort flag
@@ -266,16 +265,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
   for (int idx = 0; idx < total; ++idx) {
     const int s = idx % L::kSlots;
     const uint32_t n = static_cast<uint32_t>(idx / L::kSlots);
-    if (idx >= L::kSlots) {
-      // The slot's previous tile is released by each query tile that used it.
-      const int jp = (idx - L::kSlots) >> 1;
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (ok && jp < tl.nkv[t])
-          ok = w.wait(bar(L::bKvEmpty + t * L::kSlots + s), (n & 1u) ^ 1u, L::bKvEmpty + t * L::kSlots + s);
-      if (!ok) break;
-    }
+    if (!w.wait(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s)) break;
     mbar_arrive_expect_tx(bar(L::bKvFull + s), L::kTileBytes);
     const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
     const int row = (idx >> 1) * kBN;
@@ -296,50 +286,46 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
   }
 }
 
-// ------------------------------------------------------------ MMA warps
-// One issuing thread per query tile t (warps 13 and 14), so neither tile's
-// P*V waits behind the other tile's instructions in the tensor core's issue
-// queue. Tile t issues S_t(0), then for each key block j:
-//   O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T
-// and the two threads' streams interleave on the tensor core: it computes
-// one tile's work while the other tile's softmax runs ("FlashAttention-4"
-// §3.1.2 ping-pong). S_t(j+1) overwrites the TMEM columns that P_t(j)
-// occupies and is issued right behind the P*V that reads them by the same
-// thread: one thread's MMAs run through the SM's tensor core in issue order.
-// With FwdParams::strict_order set, S_t(j+1) instead waits for the P*V's
-// commit.
+// ------------------------------------------------------------ MMA warp
+// Issue order (two-tile ping-pong, "FlashAttention-4" §3.1.2):
+//   S_0(0), S_1(0), then for each key block j:
+//     O_0 += P_0(j) V_j, S_0(j+1) = Q_0 K_{j+1}^T, O_1 += P_1(j) V_j, S_1(j+1)
+// so the tensor core computes tile 1's work while tile 0's softmax runs and
+// the other way round. S_t(j+1) overwrites the TMEM columns that P_t(j)
+// occupies and is issued right behind the P*V that reads them: the MMAs of
+// one issuing thread run through the SM's tensor core in issue order. With
+// FwdParams::strict_order set, S_t(j+1) instead waits for the P*V's commit.
 template <int D>
-__device__ __forceinline__ void mma_role(int t, uint32_t sbase, uint32_t tmem, const Tile& tl,
+__device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Tile& tl,
                                          const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major
   constexpr uint32_t kHi = desc_hi_sw128(1024);                          // 8 rows x 128 B
-  const uint32_t col_s = t == 0 ? L::kColS0 : L::kColS1;
-  const uint32_t col_o = t == 0 ? L::kColO0 : L::kColO1;
+  const uint32_t col_s[2] = {L::kColS0, L::kColS1};
+  const uint32_t col_o[2] = {L::kColO0, L::kColO1};
   // Low descriptor halves: K-major operands (LBO unused = 16 B), V with the
   // 64-column panel stride as LBO.
-  const uint32_t q_lo = desc_lo_sw128(sbase + L::kQ + t * L::kTileBytes, 16);
+  const uint32_t q_lo[2] = {desc_lo_sw128(sbase + L::kQ, 16),
+                            desc_lo_sw128(sbase + L::kQ + L::kTileBytes, 16)};
   const uint32_t ring_lo_k = desc_lo_sw128(sbase + L::kRing, 16);
   const uint32_t ring_lo_v = desc_lo_sw128(sbase + L::kRing, L::kPanelBytes);
   constexpr uint32_t kSlotStep = L::kTileBytes >> 4;
-  const int n = tl.nkv[t];
-  if (n == 0) return;
+  if (tl.nkv_max == 0) return;
 
-  auto issue_s = [&](int slot) {
+  auto issue_s = [&](int t, int slot) {
     const uint32_t k_lo = ring_lo_k + slot * kSlotStep;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-      mma_ss_lohi(tmem + col_s, q_lo + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
+      mma_ss_lohi(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
     }
     mma_commit(bar(L::bSFull + t));
-    mma_commit(bar(L::bKvEmpty + t * L::kSlots + slot));
   };
-  // O_t += P_t V_j; each slice of P is issued once the softmax warps have
-  // stored it. Returns false on abort.
-  auto issue_pv = [&](int slot, int j) -> bool {
+  // O_t += P_t V_j in two halves of 64 keys; the second half waits for the
+  // softmax warps to have stored the second half of P. Returns false on abort.
+  auto issue_pv = [&](int t, int slot, int j) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
@@ -350,12 +336,11 @@ __device__ __forceinline__ void mma_role(int t, uint32_t sbase, uint32_t tmem, c
       for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
         // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
         const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
-        mma_ts_lohi(tmem + col_o, tmem + col_s + kk * 8, v_lo + kk * (2048 >> 4), kHi, kIdescPV,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+        mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+                    kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
     }
     mma_commit(bar(L::bPvDone + t));
-    mma_commit(bar(L::bKvEmpty + t * L::kSlots + slot));
     return true;
   };
   auto wait_slot = [&](int idx) -> bool {
@@ -368,37 +353,61 @@ __device__ __forceinline__ void mma_role(int t, uint32_t sbase, uint32_t tmem, c
 
   bool ok = w.wait(bar(L::bQ), 0u, L::bQ);
   tc_fence_after_sync();
+  // prologue: S_0(0), S_1(0)
   if (ok) ok = wait_slot(0);
   if (ok) {
-    trace_mark(p, kTrMmaSGo, 0, t);
-    issue_s(0);
-    trace_mark(p, kTrMmaSIssued, 0, t);
-  }
-  for (int j = 0; ok && j < n; ++j) {
-    const int vi = 2 * j + 1, ki = 2 * j + 2;
-    if (!(ok = wait_slot(vi))) break;
-    trace_mark(p, kTrMmaVReady, j, t);
-    trace_mark(p, kTrMmaPvWait, j, t);
-    if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t))) break;
-    tc_fence_after_sync();
-    trace_mark(p, kTrMmaPvGo, j, t);
-    if (!(ok = issue_pv(vi % L::kSlots, j))) break;
-    trace_mark(p, kTrMmaPvIssued, j, t);
-    if (j + 1 >= n) break;
-    trace_mark(p, kTrMmaSWait, j + 1, t);
-    if (!(ok = wait_slot(ki))) break;
-    if (p.strict_order) {
-      if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j) & 1u, L::bPvDone + t))) break;
-      tc_fence_after_sync();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (tl.nkv[t] == 0) continue;
+      trace_mark(p, kTrMmaSGo, 0, t);
+      issue_s(t, 0);
+      trace_mark(p, kTrMmaSIssued, 0, t);
     }
-    trace_mark(p, kTrMmaSGo, j + 1, t);
-    issue_s(ki % L::kSlots);
-    trace_mark(p, kTrMmaSIssued, j + 1, t);
-    trace_mark(p, kTrMmaCommitted, j, t);
+    mma_commit(bar(L::bKvEmpty + 0));
   }
-  // Every MMA this thread issued has completed once this commit arrives.
-  mma_commit(bar(L::bDrain + t));
-  w.drain(bar(L::bDrain + t), 0u, L::bDrain + t);
+  for (int j = 0; ok && j < tl.nkv_max; ++j) {
+    const int vi = 2 * j + 1, vs = vi % L::kSlots;
+    const int ki = 2 * j + 2, ks = ki % L::kSlots;
+    const bool next = j + 1 < tl.nkv_max;
+    if (!(ok = wait_slot(vi))) break;
+    trace_mark(p, kTrMmaVReady, j, 0);
+    bool k_ready = false;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (j >= tl.nkv[t]) continue;
+      trace_mark(p, kTrMmaPvWait, j, t);
+      if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t)))
+        break;
+      tc_fence_after_sync();
+      trace_mark(p, kTrMmaPvGo, j, t);
+      if (!(ok = issue_pv(t, vs, j))) break;
+      trace_mark(p, kTrMmaPvIssued, j, t);
+      if (j + 1 >= tl.nkv[t]) continue;
+      trace_mark(p, kTrMmaSWait, j + 1, t);
+      if (!k_ready) {
+        if (!(ok = wait_slot(ki))) break;
+        k_ready = true;
+      }
+      if (p.strict_order) {
+        if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j) & 1u, L::bPvDone + t)))
+          break;
+        tc_fence_after_sync();
+      }
+      trace_mark(p, kTrMmaSGo, j + 1, t);
+      issue_s(t, ks);
+      trace_mark(p, kTrMmaSIssued, j + 1, t);
+    }
+    if (!ok) break;
+    mma_commit(bar(L::bKvEmpty + vs));
+    if (next) {
+      // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
+      mma_commit(bar(L::bKvEmpty + ks));
+    }
+    trace_mark(p, kTrMmaCommitted, j, 0);
+  }
+  // Every MMA issued above has completed once this commit arrives.
+  mma_commit(bar(L::bDrain));
+  w.drain(bar(L::bDrain), 0u, L::bDrain);
 }
 
 // ------------------------------------------------------------ correction WG
@@ -659,7 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(bar(L::bKvFull + s), 1);
       mbar_init(bar(L::bKvEmpty + s), 1);
-      mbar_init(bar(L::bKvEmpty + L::kSlots + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::bSFull + t), 1);
@@ -671,7 +679,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bPHalf + 2 * t + 1), 4);
     }
     mbar_init(bar(L::bDrain), 1);
-    mbar_init(bar(L::bDrain + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -700,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
       load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, p, w);
-    } else if ((warp == kWarpMma || warp == kWarpMma + 1) && lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D>(warp - kWarpMma, sbase, tmem, tl, p, w);
+      mma_role<D>(sbase, tmem, tl, p, w);
     }
   }
 
