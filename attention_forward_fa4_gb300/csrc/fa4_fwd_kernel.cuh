@@ -46,8 +46,11 @@
 //   FA4_CDONE_EARLY  1: the softmax checks that the correction warps read the
 //                    previous flags while its scores load from TMEM; 0: after
 //                    the block max.
-//   FA4_WAIT_SPIN    1: waits poll with mbarrier.test_wait (no suspension);
-//                    0: mbarrier.try_wait (the thread may be suspended).
+//   FA4_WAIT_SPIN    0: waits poll mbarrier.try_wait (the thread may be
+//                    suspended for a system-dependent time); 1: poll
+//                    mbarrier.test_wait (never suspended); 2: try_wait with a
+//                    100 us suspend-time hint; 3: test_wait with a nanosleep
+//                    back-off.
 #ifndef FA4_P_SLICES
 #define FA4_P_SLICES 1
 #endif
@@ -171,8 +174,19 @@ struct Waiter {
     // 1024 failed polls.
     long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
-      if (FA4_WAIT_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
-      if ((it & 1023u) == 0u) {
+      bool done;
+      if (FA4_WAIT_SPIN == 1) {
+        done = mbar_test_wait(bar, parity);
+      } else if (FA4_WAIT_SPIN == 2) {
+        done = mbar_try_wait_hint(bar, parity, 100000u);
+      } else if (FA4_WAIT_SPIN == 3) {
+        done = mbar_test_wait(bar, parity);
+        if (!done) __nanosleep(32);
+      } else {
+        done = mbar_try_wait(bar, parity);
+      }
+      if (done) return true;
+      if ((it & (FA4_WAIT_SPIN == 2 ? 15u : 1023u)) == 0u) {
         if (honour_abort && *abort) return false;
         const long long now = clock64();
         if (t0 == 0) t0 = now;
