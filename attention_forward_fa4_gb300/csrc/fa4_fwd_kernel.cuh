@@ -49,8 +49,8 @@
 //   FA4_WAIT_SPIN    0: waits poll mbarrier.try_wait (the thread may be
 //                    suspended for a system-dependent time); 1: poll
 //                    mbarrier.test_wait (never suspended); 2: try_wait with a
-//                    100 us suspend-time hint; 3: test_wait with a nanosleep
-//                    back-off.
+//                    100 us suspend-time hint; 3, 4, 5: test_wait with a 32,
+//                    256 or 1024 ns nanosleep back-off.
 #ifndef FA4_P_SLICES
 #define FA4_P_SLICES 1
 #endif
@@ -179,9 +179,9 @@ struct Waiter {
         done = mbar_test_wait(bar, parity);
       } else if (FA4_WAIT_SPIN == 2) {
         done = mbar_try_wait_hint(bar, parity, 100000u);
-      } else if (FA4_WAIT_SPIN == 3) {
+      } else if (FA4_WAIT_SPIN >= 3) {
         done = mbar_test_wait(bar, parity);
-        if (!done) __nanosleep(32);
+        if (!done) __nanosleep(FA4_WAIT_SPIN == 3 ? 32 : (FA4_WAIT_SPIN == 4 ? 256 : 1024));
       } else {
         done = mbar_try_wait(bar, parity);
       }
