@@ -60,6 +60,13 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
+//   FA4_EXP_ROLLED   1: on blocks without masked keys the exponentials run as
+//                    a rolled loop over 32-key chunks re-read from TMEM
+//                    (double-buffered), keeping the hot loop's code small;
+//                    0: one fully unrolled pass over the row in registers.
+#ifndef FA4_EXP_ROLLED
+#define FA4_EXP_ROLLED 0
+#endif
 
 
 namespace fa4 {
@@ -489,6 +496,23 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
+// 16 entry pairs (one 32-key chunk): p = 2^(c * s - m) with FFMA2 and
+// MUFU.EX2 (or the emulation for every EMU_PAIR_PERIOD-th pair), row sum into
+// acc (fp32), BF16 pairs into pk.
+template <int EMU_PAIR_PERIOD>
+__device__ __forceinline__ void exp_chunk16(const uint32_t (&s)[32], float2 c2, float2 nm2,
+                                            float2 (&acc)[4], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                c2, nm2);
+    const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(i) ? ex2_emulated2(x)
+                                                        : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+    acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+    pk[i] = pack_bf16x2(pp.x, pp.y);
+  }
+}
+
 template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const Tile& tl, const FwdParams& p,
@@ -583,6 +607,30 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    if (FA4_EXP_ROLLED && (j + 1) * kBN <= lim_min) {
+      static_assert(!FA4_EXP_ROLLED || FA4_P_SLICES == 1, "rolled exponentials store P whole");
+      // Rolled: 32-key chunks re-read from TMEM (the scores stay intact until
+      // their own P columns are written), the next chunk's load in flight
+      // while this one is exponentiated. P chunk c goes to columns
+      // [16c, 16c + 16), which only ever overlap scores already consumed.
+      uint32_t ca[32], cb[32], pkc[16];
+      tmem_ld_x32(s_addr + 0, ca);
+#pragma unroll 1
+      for (int c = 0; c < 4; c += 2) {
+        tmem_wait_ld_x32(ca);
+        tmem_ld_x32(s_addr + 32 * (c + 1), cb);
+        exp_chunk16<EMU_PAIR_PERIOD>(ca, c2, nm2, acc, pkc);
+        tmem_st_x16(s_addr + 16 * c, pkc);
+        tmem_wait_ld_x32(cb);
+        if (c + 2 < 4) tmem_ld_x32(s_addr + 32 * (c + 2), ca);
+        exp_chunk16<EMU_PAIR_PERIOD>(cb, c2, nm2, acc, pkc);
+        tmem_st_x16(s_addr + 16 * (c + 1), pkc);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t));
+    } else {
     uint32_t pk[64];
 #pragma unroll
     for (int pi = 0; pi < 64; ++pi) {
@@ -605,6 +653,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t + half));
+    }
     }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
