@@ -52,6 +52,17 @@ unsigned int* status_ptr(int dev) {
   return static_cast<unsigned int*>(addr);
 }
 
+// Number of SMs of `dev` (looked up once each).
+int sm_count(int dev) {
+  static std::atomic<int> cache[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_acquire);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev].store(n, std::memory_order_release);
+  return n;
+}
+
 // [B, S, H, d] BF16 as a 4-D tensor (d, H, S, B); box = 64 columns x 128 rows
 // of one head, 128-byte swizzle (one swizzle row = 64 BF16).
 bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
@@ -176,8 +187,8 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
       overlaps(lse, lse_bytes, v, kv_bytes))
     return FA4_ERR_INVALID_ARG;
   const int64_t n_qblk = (static_cast<int64_t>(Sq) + 2 * kBM - 1) / (2 * kBM);
-  const int64_t grid = n_qblk * B * Hq;
-  if (grid > 0x7fffffffLL) return FA4_ERR_UNSUPPORTED;
+  const int64_t n_tiles = n_qblk * B * Hq;
+  if (n_tiles > 0x7fffffffLL) return FA4_ERR_UNSUPPORTED;
   // TMA limits: every global stride below 2^40 bytes.
   if (static_cast<uint64_t>(Sq) * Hq * d * 2 >= (1ull << 40) ||
       static_cast<uint64_t>(Sk) * Hkv * d * 2 >= (1ull << 40))
@@ -190,6 +201,11 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
   unsigned int* status = status_ptr(dev);
   if (!status) return FA4_ERR_CUDA;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return FA4_ERR_CUDA;
+  // Persistent grid: one CTA per SM (the shared-memory footprint allows no
+  // more), each visiting work tiles blockIdx.x, blockIdx.x + grid, ...
+  const int64_t grid = n_tiles < sms ? n_tiles : sms;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (Sk == 0) {  // no keys: O = 0, LSE = -inf
@@ -213,6 +229,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.Sk = Sk;
   p.group = Hq / Hkv;
   p.n_qblk = static_cast<int>(n_qblk);
+  p.n_tiles = static_cast<int>(n_tiles);
   // Causal tiles run heaviest first across a chunk of heads whose K/V stay
   // resident in L2; non-causal tiles of one head run side by side.
   p.head_chunk = causal ? (B * Hq < 8 ? B * Hq : 8) : 1;

@@ -1,7 +1,8 @@
 // fa4_fwd_kernel.cuh -- warp-specialised attention forward for sm_103a.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) -- M = 256 rows
-// -- and walks every key block of 128 keys once ("FlashAttention-4:
+// A work tile is two 128-row query tiles of one (batch, head) -- M = 256
+// rows -- walking every key block of 128 keys once; a persistent grid of
+// one CTA per SM visits the work tiles in turn ("FlashAttention-4:
 // Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware
 // Scaling", Table 1 / §3.1.1 tile M = 256, N = 128; §3.1.2 two output
 // tiles per CTA). Roles, one per warp group (§3.1.2, Method (1); "How
@@ -60,13 +61,6 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
-//   FA4_EXP_ROLLED   1: on blocks without masked keys the exponentials run as
-//                    a rolled loop over 32-key chunks re-read from TMEM
-//                    (double-buffered), keeping the hot loop's code small;
-//                    0: one fully unrolled pass over the row in registers.
-#ifndef FA4_EXP_ROLLED
-#define FA4_EXP_ROLLED 0
-#endif
 
 
 namespace fa4 {
@@ -97,12 +91,14 @@ struct FwdParams {
   unsigned long long* trace;   // optional per-role cycle trace (see trace_mark)
   int trace_ctas;              // CTAs (by blockIdx.x) that record a trace
   int strict_order;            // 1: S_t(j+1) waits for P_t(j) V_j to complete
+  int n_tiles;                 // n_qblk * B * Hq work tiles, visited by a persistent grid
 };
 
 // ------------------------------------------------------------ cycle trace
 // Optional diagnostic: when FwdParams::trace is set, CTAs with
 // blockIdx.x < trace_ctas record the SM cycle counter at fixed points of
-// each role, for key block j < kTraceSteps and query tile t:
+// each role, for key block j < kTraceSteps and query tile t of the CTA's
+// first work tile:
 //   trace[((cta * kTraceEvents + event) * kTraceSteps + j) * 2 + t].
 // The MMA thread, lane 0 of the first softmax warp of each tile and lane 0
 // of the first correction warp record. A null pointer costs one uniform
@@ -131,8 +127,8 @@ enum TraceEvent : int {
   kTraceEvents
 };
 
-__device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, int t) {
-  if (p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas && j < kTraceSteps) {
+__device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, int t, int iter = 0) {
+  if (p.trace != nullptr && iter == 0 && static_cast<int>(blockIdx.x) < p.trace_ctas && j < kTraceSteps) {
     uint64_t c;
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
     p.trace[((static_cast<size_t>(blockIdx.x) * kTraceEvents + ev) * kTraceSteps + j) * 2 + t] = c;
@@ -158,7 +154,9 @@ struct Smem {
   static constexpr int bPvDone = bOReady + 2;            // [2]
   static constexpr int bCDone = bPvDone + 2;             // [2]
   static constexpr int bPHalf = bCDone + 2;              // [2 tiles][2 halves]
-  static constexpr int bDrain = bPHalf + 4;
+  static constexpr int bQEmpty = bPHalf + 4;             // Q tiles free for the next work tile
+  static constexpr int bOFree = bQEmpty + 1;             // [2] epilogue has read O_t
+  static constexpr int bDrain = bOFree + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
   static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
@@ -222,6 +220,8 @@ struct Waiter {
 };
 
 // ------------------------------------------------------------ tile geometry
+// A work tile is two 128-row query tiles of one (batch, head). The grid is
+// persistent: CTA c visits work tiles c, c + gridDim.x, c + 2 gridDim.x, ...
 struct Tile {
   int b, h, hk, q0;
   int nkv[2];       // key blocks each query tile visits
@@ -229,11 +229,10 @@ struct Tile {
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ Tile make_tile(const FwdParams& p) {
+__device__ __forceinline__ Tile make_tile(const FwdParams& p, int id) {
   Tile tl;
   const int n_bh = p.B * p.Hq;
   const int per_chunk = p.head_chunk * p.n_qblk;
-  const int id = static_cast<int>(blockIdx.x);
   const int chunk = id / per_chunk;
   const int rem = id - chunk * per_chunk;
   const int g_eff = min(p.head_chunk, n_bh - chunk * p.head_chunk);
@@ -267,40 +266,51 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p) {
 }
 
 // ------------------------------------------------------------ load warp
-template <int D>
+// Q once per work tile (after the previous tile's S MMAs have released the
+// Q buffers), then K_j, V_j of every key block into the slot ring; the
+// ring's fill counter runs on across work tiles.
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, uint32_t sbase,
-                                          const Tile& tl, const FwdParams& p, const Waiter& w) {
+                                          const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  if (tl.nkv_max == 0) return;
-  mbar_arrive_expect_tx(bar(L::bQ), 2u * L::kTileBytes);
+  int fill = 0;     // K/V copies issued so far (ring position)
+  int n_q = 0;      // Q copies issued so far
+  bool ok = true;
+  int iter = 0;
+  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+    const Tile tl = make_tile<CAUSAL>(p, id);
+    if (tl.nkv_max == 0) continue;
+    if (n_q > 0 && !(ok = w.wait(bar(L::bQEmpty), static_cast<uint32_t>(n_q - 1) & 1u, L::bQEmpty)))
+      break;
+    mbar_arrive_expect_tx(bar(L::bQ), 2u * L::kTileBytes);
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
+    for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int pn = 0; pn < L::kPanels; ++pn)
-      tma_load_4d(sbase + L::kQ + t * L::kTileBytes + pn * L::kPanelBytes, tm_q, bar(L::bQ),
-                  pn * 64, tl.h, tl.q0 + t * kBM, tl.b);
-  const int total = 2 * tl.nkv_max;   // K_0, V_0, K_1, V_1, ...
-  int issued = 0;
-  for (int idx = 0; idx < total; ++idx) {
-    const int s = idx % L::kSlots;
-    const uint32_t n = static_cast<uint32_t>(idx / L::kSlots);
-    if (!w.wait(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s)) break;
-    mbar_arrive_expect_tx(bar(L::bKvFull + s), L::kTileBytes);
-    const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
-    const int row = (idx >> 1) * kBN;
+      for (int pn = 0; pn < L::kPanels; ++pn)
+        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + pn * L::kPanelBytes, tm_q, bar(L::bQ),
+                    pn * 64, tl.h, tl.q0 + t * kBM, tl.b);
+    ++n_q;
+    for (int idx = 0; idx < 2 * tl.nkv_max; ++idx) {   // K_0, V_0, K_1, V_1, ...
+      const int s = fill % L::kSlots;
+      const uint32_t n = static_cast<uint32_t>(fill / L::kSlots);
+      if (!(ok = w.wait(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s))) break;
+      mbar_arrive_expect_tx(bar(L::bKvFull + s), L::kTileBytes);
+      const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
+      const int row = (idx >> 1) * kBN;
 #pragma unroll
-    for (int pn = 0; pn < L::kPanels; ++pn)
-      tma_load_4d(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm, bar(L::bKvFull + s),
-                  pn * 64, tl.hk, row, tl.b);
-    issued = idx + 1;
-    trace_mark(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1);
+      for (int pn = 0; pn < L::kPanels; ++pn)
+        tma_load_4d(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm,
+                    bar(L::bKvFull + s), pn * 64, tl.hk, row, tl.b);
+      ++fill;
+      trace_mark(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1, iter);
+    }
   }
-  if (issued < total || *w.abort) {
+  if (!ok || *w.abort) {
     // Let every copy this warp started land before the CTA frees its memory.
-    w.drain(bar(L::bQ), 0u, L::bQ);
-    for (int idx = max(0, issued - L::kSlots); idx < issued; ++idx) {
+    if (n_q > 0) w.drain(bar(L::bQ), static_cast<uint32_t>(n_q - 1) & 1u, L::bQ);
+    for (int idx = max(0, fill - L::kSlots); idx < fill; ++idx) {
       const int s = idx % L::kSlots;
       w.drain(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u, L::bKvFull + s);
     }
@@ -316,9 +326,13 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // occupies and is issued right behind the P*V that reads them: the MMAs of
 // one issuing thread run through the SM's tensor core in issue order. With
 // FwdParams::strict_order set, S_t(j+1) instead waits for the P*V's commit.
-template <int D>
-__device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Tile& tl,
-                                         const FwdParams& p, const Waiter& w) {
+//
+// Phases run on across the CTA's work tiles: the ring position, the count
+// of P*V MMAs per query tile and the count of earlier tiles whose O_t the
+// epilogue has to read before the next tile's first P*V overwrites it.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const FwdParams& p,
+                                         const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
@@ -333,7 +347,6 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
   const uint32_t ring_lo_k = desc_lo_sw128(sbase + L::kRing, 16);
   const uint32_t ring_lo_v = desc_lo_sw128(sbase + L::kRing, L::kPanelBytes);
   constexpr uint32_t kSlotStep = L::kTileBytes >> 4;
-  if (tl.nkv_max == 0) return;
 
   auto issue_s = [&](int t, int slot) {
     const uint32_t k_lo = ring_lo_k + slot * kSlotStep;
@@ -344,13 +357,14 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
     }
     mma_commit(bar(L::bSFull + t));
   };
-  // O_t += P_t V_j in two halves of 64 keys; the second half waits for the
-  // softmax warps to have stored the second half of P. Returns false on abort.
-  auto issue_pv = [&](int t, int slot, int j) -> bool {
+  // O_t (+)= P_t V; each slice of P is issued once the softmax warps have
+  // stored it. `phase` counts this tile's earlier P*V MMAs. Returns false on
+  // abort.
+  auto issue_pv = [&](int t, int slot, bool first, int phase) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
-      if (!w.wait(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(j) & 1u, L::bPHalf + 2 * t + half))
+      if (!w.wait(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
 #pragma unroll
@@ -358,73 +372,96 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
         // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
         const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
         mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
-                    kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    kIdescPV, (!first || kk > 0) ? 1u : 0u);
       }
     }
     mma_commit(bar(L::bPvDone + t));
     return true;
   };
-  auto wait_slot = [&](int idx) -> bool {
-    const int s = idx % L::kSlots;
-    const bool ok = w.wait(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u,
+  auto wait_slot = [&](int pos) -> bool {
+    const int s = pos % L::kSlots;
+    const bool ok = w.wait(bar(L::bKvFull + s), static_cast<uint32_t>(pos / L::kSlots) & 1u,
                            L::bKvFull + s);
     tc_fence_after_sync();
     return ok;
   };
 
-  bool ok = w.wait(bar(L::bQ), 0u, L::bQ);
-  tc_fence_after_sync();
-  // prologue: S_0(0), S_1(0)
-  if (ok) ok = wait_slot(0);
-  if (ok) {
+  int cons = 0;                 // ring positions consumed
+  int n_q = 0;                  // Q tile pairs consumed
+  int n_pv[2] = {0, 0};         // P*V MMAs issued per query tile
+  int n_epi[2] = {0, 0};        // earlier work tiles whose O_t the epilogue reads
+  bool ok = true;
+  int iter = 0;
+  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+    const Tile tl = make_tile<CAUSAL>(p, id);
+    if (tl.nkv_max == 0) continue;
+    if (!(ok = w.wait(bar(L::bQ), static_cast<uint32_t>(n_q) & 1u, L::bQ))) break;
+    tc_fence_after_sync();
+    ++n_q;
+    // S_0(0), S_1(0)
+    if (!(ok = wait_slot(cons))) break;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (tl.nkv[t] == 0) continue;
-      trace_mark(p, kTrMmaSGo, 0, t);
-      issue_s(t, 0);
-      trace_mark(p, kTrMmaSIssued, 0, t);
+      trace_mark(p, kTrMmaSGo, 0, t, iter);
+      issue_s(t, cons % L::kSlots);
+      trace_mark(p, kTrMmaSIssued, 0, t, iter);
     }
-    mma_commit(bar(L::bKvEmpty + 0));
-  }
-  for (int j = 0; ok && j < tl.nkv_max; ++j) {
-    const int vi = 2 * j + 1, vs = vi % L::kSlots;
-    const int ki = 2 * j + 2, ks = ki % L::kSlots;
-    const bool next = j + 1 < tl.nkv_max;
-    if (!(ok = wait_slot(vi))) break;
-    trace_mark(p, kTrMmaVReady, j, 0);
-    bool k_ready = false;
+    mma_commit(bar(L::bKvEmpty + cons % L::kSlots));
+    ++cons;
+    if (tl.nkv_max == 1) mma_commit(bar(L::bQEmpty));     // no further S of this tile
+    for (int j = 0; ok && j < tl.nkv_max; ++j) {
+      const int vpos = cons, kpos = cons + 1;             // V_j, then K_{j+1}
+      const bool next = j + 1 < tl.nkv_max;
+      if (!(ok = wait_slot(vpos))) break;
+      trace_mark(p, kTrMmaVReady, j, 0, iter);
+      bool k_ready = false;
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      if (j >= tl.nkv[t]) continue;
-      trace_mark(p, kTrMmaPvWait, j, t);
-      if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(j) & 1u, L::bOReady + t)))
-        break;
-      tc_fence_after_sync();
-      trace_mark(p, kTrMmaPvGo, j, t);
-      if (!(ok = issue_pv(t, vs, j))) break;
-      trace_mark(p, kTrMmaPvIssued, j, t);
-      if (j + 1 >= tl.nkv[t]) continue;
-      trace_mark(p, kTrMmaSWait, j + 1, t);
-      if (!k_ready) {
-        if (!(ok = wait_slot(ki))) break;
-        k_ready = true;
-      }
-      if (p.strict_order) {
-        if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j) & 1u, L::bPvDone + t)))
+      for (int t = 0; t < 2; ++t) {
+        if (j >= tl.nkv[t]) continue;
+        trace_mark(p, kTrMmaPvWait, j, t, iter);
+        if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
+          break;
+        if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
+            !(ok = w.wait(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
           break;
         tc_fence_after_sync();
+        trace_mark(p, kTrMmaPvGo, j, t, iter);
+        if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t]))) break;
+        ++n_pv[t];
+        trace_mark(p, kTrMmaPvIssued, j, t, iter);
+        if (j + 1 >= tl.nkv[t]) continue;
+        trace_mark(p, kTrMmaSWait, j + 1, t, iter);
+        if (!k_ready) {
+          if (!(ok = wait_slot(kpos))) break;
+          k_ready = true;
+        }
+        if (p.strict_order) {
+          if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_pv[t] - 1) & 1u,
+                            L::bPvDone + t)))
+            break;
+          tc_fence_after_sync();
+        }
+        trace_mark(p, kTrMmaSGo, j + 1, t, iter);
+        issue_s(t, kpos % L::kSlots);
+        trace_mark(p, kTrMmaSIssued, j + 1, t, iter);
       }
-      trace_mark(p, kTrMmaSGo, j + 1, t);
-      issue_s(t, ks);
-      trace_mark(p, kTrMmaSIssued, j + 1, t);
+      if (!ok) break;
+      mma_commit(bar(L::bKvEmpty + vpos % L::kSlots));
+      ++cons;
+      if (next) {
+        // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
+        mma_commit(bar(L::bKvEmpty + kpos % L::kSlots));
+        ++cons;
+      }
+      // The last S MMAs of this work tile are issued: once they complete the
+      // Q buffers may take the next tile's queries.
+      if (j + 2 == tl.nkv_max) mma_commit(bar(L::bQEmpty));
+      trace_mark(p, kTrMmaCommitted, j, 0, iter);
     }
-    if (!ok) break;
-    mma_commit(bar(L::bKvEmpty + vs));
-    if (next) {
-      // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
-      mma_commit(bar(L::bKvEmpty + ks));
-    }
-    trace_mark(p, kTrMmaCommitted, j, 0);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (tl.nkv[t] > 0) ++n_epi[t];
   }
   // Every MMA issued above has completed once this commit arrives.
   mma_commit(bar(L::bDrain));
@@ -432,10 +469,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Ti
 }
 
 // ------------------------------------------------------------ correction WG
-template <int D>
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                                                const Tile& tl, const FwdParams& p,
-                                                const Waiter& w) {
+                                                const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -445,40 +481,46 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
   const volatile int* flags_s = reinterpret_cast<const volatile int*>(smem + L::kFlags);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
-  for (int j = 0; j < tl.nkv_max; ++j) {
+  int n_step[2] = {0, 0};       // softmax steps seen per query tile (all work tiles)
+  int iter = 0;
+  for (int id = blockIdx.x; id < p.n_tiles; id += gridDim.x, ++iter) {
+    const Tile tl = make_tile<CAUSAL>(p, id);
+    for (int j = 0; j < tl.nkv_max; ++j) {
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      if (j >= tl.nkv[t]) continue;
-      if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(j) & 1u, L::bPFull + t)) return;
-      tc_fence_after_sync();
-      if (warp == 8 && lane == 0) trace_mark(p, kTrCoWake, j, t);
-      const bool flagged = j > 0 && flags_s[t * 4 + wq] != 0;
-      const float a = flagged ? alpha_s[t * kBM + r] : 1.0f;
-      // flags and alpha of step j are read: the softmax may overwrite them
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bCDone + t));
-      if (flagged) {
-        // This 32-row group's reference max moved: O_t <- alpha * O_t once
-        // the previous P*V into O_t has completed, then release the group.
-        if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bPvDone + t))
-          return;
+      for (int t = 0; t < 2; ++t) {
+        if (j >= tl.nkv[t]) continue;
+        const int cnt = n_step[t]++;
+        if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
         tc_fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t x[16];
-          const uint32_t addr = lane_base + col_o[t] + c * 16;
-          tmem_ld_x16(addr, x);
-          tmem_wait_ld_x16(x);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * a);
-          tmem_st_x16(addr, x);
-        }
-        tmem_wait_st();
-        tc_fence_before_sync();
+        if (warp == 8 && lane == 0) trace_mark(p, kTrCoWake, j, t, iter);
+        const bool flagged = j > 0 && flags_s[t * 4 + wq] != 0;
+        const float a = flagged ? alpha_s[t * kBM + r] : 1.0f;
+        // flags and alpha of this step are read: the softmax may overwrite them
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bOReady + t));
+        if (lane == 0) mbar_arrive(bar(L::bCDone + t));
+        if (flagged) {
+          // This 32-row group's reference max moved: O_t <- alpha * O_t once
+          // the previous P*V into O_t has completed, then release the group.
+          if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
+            return;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t x[16];
+            const uint32_t addr = lane_base + col_o[t] + c * 16;
+            tmem_ld_x16(addr, x);
+            tmem_wait_ld_x16(x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * a);
+            tmem_st_x16(addr, x);
+          }
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::bOReady + t));
+        }
+        if (warp == 8 && lane == 0) trace_mark(p, kTrCoArrived, j, t, iter);
       }
-      if (warp == 8 && lane == 0) trace_mark(p, kTrCoArrived, j, t);
     }
   }
 }
@@ -496,56 +538,41 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
-// 16 entry pairs (one 32-key chunk): p = 2^(c * s - m) with FFMA2 and
-// MUFU.EX2 (or the emulation for every EMU_PAIR_PERIOD-th pair), row sum into
-// acc (fp32), BF16 pairs into pk.
-template <int EMU_PAIR_PERIOD>
-__device__ __forceinline__ void exp_chunk16(const uint32_t (&s)[32], float2 c2, float2 nm2,
-                                            float2 (&acc)[4], uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                c2, nm2);
-    const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(i) ? ex2_emulated2(x)
-                                                        : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-    acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-    pk[i] = pack_bf16x2(pp.x, pp.y);
-  }
-}
-
 template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                                             const Tile& tl, const FwdParams& p,
-                                             const Waiter& w) {
+                                             const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
   const int r = wq * 32 + lane;                 // row within the tile = TMEM lane
-  const int row = tl.q0 + t * kBM + r;          // query index
   float* alpha_s = reinterpret_cast<float*>(smem + L::kAlpha);
   volatile int* flags_s = reinterpret_cast<volatile int*>(smem + L::kFlags);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t s_addr = lane_base + (t == 0 ? L::kColS0 : L::kColS1);
   const uint32_t o_addr = lane_base + (t == 0 ? L::kColO0 : L::kColO1);
-  const int n = tl.nkv[t];
   const float cl2 = p.scale_log2;
-  // Keys k < lim_row are visible to this row; lim_min is the tile's smallest.
   const int shift = p.Sk - p.Sq;
+  unsigned n_rescaled = 0, n_steps = 0;
+  int n_step = 0;               // steps of this query tile over all work tiles
+  bool ok = true;
+  int iter = 0;
+  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+  const Tile tl = make_tile<CAUSAL>(p, id);
+  const int row = tl.q0 + t * kBM + r;          // query index
+  const int n = tl.nkv[t];
+  // Keys k < lim_row are visible to this row; lim_min is the tile's smallest.
   const int lim_row = CAUSAL ? max(0, min(p.Sk, row + shift + 1)) : p.Sk;
   const int row_min = tl.q0 + t * kBM;
   const int lim_min = CAUSAL ? max(0, min(p.Sk, row_min + shift + 1)) : p.Sk;
-
   float m_ref = -INFINITY;      // reference max (log2 units) of the last rescale
   float l = 0.0f;               // running sum of p relative to m_ref
-  unsigned n_rescaled = 0, n_steps = 0;
-  bool ok = true;
 
   for (int j = 0; j < n; ++j) {
-    if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(j) & 1u, L::bSFull + t))) break;
+    if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
     tc_fence_after_sync();
     const bool tracer = (wq == 0 && lane == 0);
-    if (tracer) trace_mark(p, kTrSmSReady, j, t);
+    if (tracer) trace_mark(p, kTrSmSReady, j, t, iter);
     uint32_t s[128];
     tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
@@ -553,14 +580,14 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     // The correction warps must have read the flags / alpha of step j-1
     // before they are overwritten (normally long done).
-    if (FA4_CDONE_EARLY && j > 0 &&
-        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+    if (FA4_CDONE_EARLY && n_step > 0 &&
+        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bCDone + t)))
       break;
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    if (tracer) trace_mark(p, kTrSmLoaded, j, t);
+    if (tracer) trace_mark(p, kTrSmLoaded, j, t, iter);
     if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
       const int lim = lim_row - j * kBN;                 // this row's first masked column
 #pragma unroll
@@ -579,10 +606,10 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
     // than tau, decided per warp so the correction stays warp-uniform.
     const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-    if (!FA4_CDONE_EARLY && j > 0 &&
-        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(j - 1) & 1u, L::bCDone + t)))
+    if (!FA4_CDONE_EARLY && n_step > 0 &&
+        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bCDone + t)))
       break;
-    if (tracer) trace_mark(p, kTrSmMaxDone, j, t);
+    if (tracer) trace_mark(p, kTrSmMaxDone, j, t, iter);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
       l *= alpha;
@@ -607,30 +634,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    if (FA4_EXP_ROLLED && (j + 1) * kBN <= lim_min) {
-      static_assert(!FA4_EXP_ROLLED || FA4_P_SLICES == 1, "rolled exponentials store P whole");
-      // Rolled: 32-key chunks re-read from TMEM (the scores stay intact until
-      // their own P columns are written), the next chunk's load in flight
-      // while this one is exponentiated. P chunk c goes to columns
-      // [16c, 16c + 16), which only ever overlap scores already consumed.
-      uint32_t ca[32], cb[32], pkc[16];
-      tmem_ld_x32(s_addr + 0, ca);
-#pragma unroll 1
-      for (int c = 0; c < 4; c += 2) {
-        tmem_wait_ld_x32(ca);
-        tmem_ld_x32(s_addr + 32 * (c + 1), cb);
-        exp_chunk16<EMU_PAIR_PERIOD>(ca, c2, nm2, acc, pkc);
-        tmem_st_x16(s_addr + 16 * c, pkc);
-        tmem_wait_ld_x32(cb);
-        if (c + 2 < 4) tmem_ld_x32(s_addr + 32 * (c + 2), ca);
-        exp_chunk16<EMU_PAIR_PERIOD>(cb, c2, nm2, acc, pkc);
-        tmem_st_x16(s_addr + 16 * (c + 1), pkc);
-      }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t));
-    } else {
     uint32_t pk[64];
 #pragma unroll
     for (int pi = 0; pi < 64; ++pi) {
@@ -654,40 +657,42 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t + half));
     }
-    }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
-    if (tracer) trace_mark(p, kTrSmExpDone, j, t);
-    if (tracer) trace_mark(p, kTrSmArrived, j, t);
-    if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t);
+    if (tracer) trace_mark(p, kTrSmExpDone, j, t, iter);
+    if (tracer) trace_mark(p, kTrSmArrived, j, t, iter);
+    if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
+    ++n_step;
   }
 
+  if (!ok) break;
   // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l)
-  if (ok && n > 0) {
-    ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n - 1) & 1u, L::bPvDone + t);
-    tc_fence_after_sync();
-  }
-  if (!ok) return;
   const bool row_valid = row < p.Sq;
   const bool has_keys = n > 0 && m_ref != -INFINITY;
   const float inv_l = has_keys ? 1.0f / l : 0.0f;
   __nv_bfloat16* orow =
       p.o + ((static_cast<int64_t>(tl.b) * p.Sq + row) * p.Hq + tl.h) * static_cast<int64_t>(D);
   if (n > 0) {
+    if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
+      break;
+    tc_fence_after_sync();
+    uint32_t x[D];
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t x[32];
-      tmem_ld_x32(o_addr + c * 32, x);
-      tmem_wait_ld_x32(x);
-      if (row_valid) {
-        uint32_t pkd[16];
+    for (int c = 0; c < D / 32; ++c) tmem_ld_x32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pkd[i] = pack_bf16x2(__uint_as_float(x[2 * i]) * inv_l, __uint_as_float(x[2 * i + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+    for (int c = 0; c < D / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+    // O_t is in registers: the next work tile's first P*V may overwrite it.
+    tc_fence_before_sync();
+    mbar_arrive(bar(L::bOFree + t));
+    if (row_valid) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(x[8 * c + 0]) * inv_l, __uint_as_float(x[8 * c + 1]) * inv_l);
+        v.y = pack_bf16x2(__uint_as_float(x[8 * c + 2]) * inv_l, __uint_as_float(x[8 * c + 3]) * inv_l);
+        v.z = pack_bf16x2(__uint_as_float(x[8 * c + 4]) * inv_l, __uint_as_float(x[8 * c + 5]) * inv_l);
+        v.w = pack_bf16x2(__uint_as_float(x[8 * c + 6]) * inv_l, __uint_as_float(x[8 * c + 7]) * inv_l);
+        reinterpret_cast<uint4*>(orow)[c] = v;
       }
     }
   } else if (row_valid) {
@@ -699,6 +704,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     p.lse[(static_cast<int64_t>(tl.b) * p.Hq + tl.h) * p.Sq + row] =
         has_keys ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
   }
+  }  // work tiles
   if (p.stats != nullptr && lane == 0 && n_steps > 0) {
     atomicAdd(&p.stats[0], static_cast<unsigned long long>(n_rescaled));
     atomicAdd(&p.stats[1], static_cast<unsigned long long>(n_steps));
@@ -720,8 +726,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const Tile tl = make_tile<CAUSAL>(p);
-
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -740,7 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bCDone + t), 4);
       mbar_init(bar(L::bPHalf + 2 * t), 4);
       mbar_init(bar(L::bPHalf + 2 * t + 1), 4);
+      mbar_init(bar(L::bOFree + t), kBM);
     }
+    mbar_init(bar(L::bQEmpty), 1);
     mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -760,19 +766,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     regs_increase<176>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, tl, p, w);
+    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, p, w);
   } else if (warp < 12) {
     regs_decrease<72>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D>(sbase, smem, tmem, tl, p, w);
+    correction_role<D, CAUSAL>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<88>();
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      load_role<D>(&tm_q, &tm_k, &tm_v, sbase, tl, p, w);
+      load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, p, w);
     } else if (warp == kWarpMma && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D>(sbase, tmem, tl, p, w);
+      mma_role<D, CAUSAL>(sbase, tmem, p, w);
     }
   }
 
