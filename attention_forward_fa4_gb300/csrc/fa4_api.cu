@@ -230,9 +230,10 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.group = Hq / Hkv;
   p.n_qblk = static_cast<int>(n_qblk);
   p.n_tiles = static_cast<int>(n_tiles);
-  // Causal tiles run heaviest first across a chunk of heads whose K/V stay
-  // resident in L2; non-causal tiles of one head run side by side.
-  p.head_chunk = causal ? (B * Hq < 8 ? B * Hq : 8) : 1;
+  // Causal tiles are numbered heaviest first over all heads (the snake
+  // assignment of the persistent grid balances them); non-causal tiles of
+  // one head are numbered side by side so their K/V reads meet in L2.
+  p.head_chunk = causal ? B * Hq : 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = op.tau;
   p.stats = op.rescale_stats;

@@ -221,7 +221,15 @@ struct Waiter {
 
 // ------------------------------------------------------------ tile geometry
 // A work tile is two 128-row query tiles of one (batch, head). The grid is
-// persistent: CTA c visits work tiles c, c + gridDim.x, c + 2 gridDim.x, ...
+// persistent: with G = gridDim.x, CTA c visits work tiles in snake order
+// c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... Causal tiles are numbered heaviest
+// first, so the pairs a CTA takes from consecutive rounds add up to about
+// the same work on every CTA.
+__device__ __forceinline__ int tile_of(int k) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+
 struct Tile {
   int b, h, hk, q0;
   int nkv[2];       // key blocks each query tile visits
@@ -279,7 +287,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
   int n_q = 0;      // Q copies issued so far
   bool ok = true;
   int iter = 0;
-  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     if (tl.nkv_max == 0) continue;
     if (n_q > 0 && !(ok = w.wait(bar(L::bQEmpty), static_cast<uint32_t>(n_q - 1) & 1u, L::bQEmpty)))
@@ -392,7 +400,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   int n_epi[2] = {0, 0};        // earlier work tiles whose O_t the epilogue reads
   bool ok = true;
   int iter = 0;
-  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     if (tl.nkv_max == 0) continue;
     if (!(ok = w.wait(bar(L::bQ), static_cast<uint32_t>(n_q) & 1u, L::bQ))) break;
@@ -483,7 +491,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
   int n_step[2] = {0, 0};       // softmax steps seen per query tile (all work tiles)
   int iter = 0;
-  for (int id = blockIdx.x; id < p.n_tiles; id += gridDim.x, ++iter) {
+  for (int id = tile_of(0); id < p.n_tiles; id = tile_of(++iter)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     for (int j = 0; j < tl.nkv_max; ++j) {
 #pragma unroll
@@ -557,7 +565,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   int n_step = 0;               // steps of this query tile over all work tiles
   bool ok = true;
   int iter = 0;
-  for (int id = blockIdx.x; ok && id < p.n_tiles; id += gridDim.x, ++iter) {
+  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
   const Tile tl = make_tile<CAUSAL>(p, id);
   const int row = tl.q0 + t * kBM + r;          // query index
   const int n = tl.nkv[t];
