@@ -47,7 +47,8 @@ class Fa4Error(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("exp2_emulation", ctypes.c_int),
                 ("rescale_stats", ctypes.c_void_p), ("trace", ctypes.c_void_p),
-                ("trace_ctas", ctypes.c_int), ("strict_mma_order", ctypes.c_int)]
+                ("trace_ctas", ctypes.c_int), ("strict_mma_order", ctypes.c_int),
+                ("grid_mode", ctypes.c_int)]
 
 
 TRACE_EVENTS = 19
@@ -111,7 +112,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              tau: float = 8.0, exp2_emulation: bool = True,
              rescale_stats: Optional[torch.Tensor] = None,
              trace: Optional[torch.Tensor] = None, strict_mma_order: bool = False,
-             stream: Optional[torch.cuda.Stream] = None) -> None:
+             grid_mode: int = 0, stream: Optional[torch.cuda.Stream] = None) -> None:
     """Write attention forward into preallocated ``o`` and ``lse``.
 
     Shapes: q, o [B,Sq,Hq,d]; k, v [B,Sk,Hkv,d] (BF16, contiguous, CUDA);
@@ -140,6 +141,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     opt.tau = float(tau)
     opt.exp2_emulation = 1 if exp2_emulation else 0
     opt.strict_mma_order = 1 if strict_mma_order else 0
+    opt.grid_mode = int(grid_mode)
     if rescale_stats is not None:
         if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
             raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")

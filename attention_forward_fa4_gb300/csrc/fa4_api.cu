@@ -52,6 +52,14 @@ unsigned int* status_ptr(int dev) {
   return static_cast<unsigned int*>(addr);
 }
 
+// Automatic grid choice: the persistent grid pays off when work tiles are
+// short (few key blocks each), where per-CTA start-up is a large share of a
+// tile; long tiles keep one CTA per tile and the hardware's dynamic dispatch.
+bool use_persistent_grid(int64_t n_tiles, int sms, int nblk, bool causal) {
+  (void)causal;
+  return n_tiles > sms && nblk <= 8;
+}
+
 // Number of SMs of `dev` (looked up once each).
 int sm_count(int dev) {
   static std::atomic<int> cache[kMaxDevices];
@@ -135,6 +143,7 @@ void fa4_fwd_default_options(fa4_fwd_options* opt) {
   opt->trace = nullptr;
   opt->trace_ctas = 0;
   opt->strict_mma_order = 0;
+  opt->grid_mode = 0;
 }
 
 const char* fa4_status_string(fa4_status s) {
@@ -167,6 +176,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (!std::isfinite(op.tau) || op.tau < 0.0f || op.tau > 64.0f) return FA4_ERR_INVALID_ARG;
   if (op.exp2_emulation != 0 && op.exp2_emulation != 1) return FA4_ERR_INVALID_ARG;
   if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
+  if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) return FA4_OK;  // empty output: nothing to do
   if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
@@ -203,9 +213,19 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (!status) return FA4_ERR_CUDA;
   const int sms = sm_count(dev);
   if (sms <= 0) return FA4_ERR_CUDA;
-  // Persistent grid: one CTA per SM (the shared-memory footprint allows no
-  // more), each visiting work tiles blockIdx.x, blockIdx.x + grid, ...
-  const int64_t grid = n_tiles < sms ? n_tiles : sms;
+  // Grid: one CTA per work tile (the hardware hands the next tile to the
+  // first free SM), or persistent (one CTA per SM -- the shared-memory
+  // footprint allows no more -- walking its tiles in snake order).
+  const int nblk = (Sk + 2 * kBM - 1) / kBN;   // key blocks of the longest query tile (upper bound)
+  bool persistent;
+  if (op.grid_mode == 1) {
+    persistent = false;
+  } else if (op.grid_mode == 2) {
+    persistent = true;
+  } else {
+    persistent = use_persistent_grid(n_tiles, sms, nblk, causal != 0);
+  }
+  const int64_t grid = persistent ? (n_tiles < sms ? n_tiles : sms) : n_tiles;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (Sk == 0) {  // no keys: O = 0, LSE = -inf
@@ -230,10 +250,12 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.group = Hq / Hkv;
   p.n_qblk = static_cast<int>(n_qblk);
   p.n_tiles = static_cast<int>(n_tiles);
-  // Causal tiles are numbered heaviest first over all heads (the snake
-  // assignment of the persistent grid balances them); non-causal tiles of
-  // one head are numbered side by side so their K/V reads meet in L2.
-  p.head_chunk = causal ? B * Hq : 1;
+  // Causal tiles are numbered heaviest first: over all heads for the
+  // persistent grid (its snake assignment balances them), within chunks of 8
+  // (batch, head) pairs whose K/V stay in L2 when the hardware schedules one
+  // CTA per tile. Non-causal tiles of one head are numbered side by side so
+  // their K/V reads meet in L2.
+  p.head_chunk = causal ? (persistent ? B * Hq : (B * Hq < 8 ? B * Hq : 8)) : 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = op.tau;
   p.stats = op.rescale_stats;

@@ -92,13 +92,18 @@ typedef struct {
      * the P_t*V MMA to complete first (slower; the PTX memory model only
      * promises issue order for MMAs into the same accumulator). */
     int strict_mma_order;
+    /* Grid of CTAs: 0 (default) chooses automatically; 1: one CTA per work
+     * tile (two 128-row query tiles of one batch and head), scheduled by the
+     * hardware; 2: persistent, one CTA per SM, each taking work tiles in
+     * snake order. Both compute identical results. */
+    int grid_mode;
 } fa4_fwd_options;
 
 #define FA4_TRACE_EVENTS 19
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 1, no counters, no trace,
- * strict_mma_order = 0. */
+ * strict_mma_order = 0, grid_mode = 0. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 
 /*

@@ -195,3 +195,17 @@ def test_back_to_back_issue_equals_strict_order(shape):
     for _ in range(5):
         o_f, l_f = _run(q, k, v, causal)
         assert torch.equal(o_f, o_s) and torch.equal(l_f, l_s)
+
+
+# ------------------------------------------------------------ grid modes
+@pytest.mark.parametrize("shape", [(2, 8, 8, 2048, 2048, 128, True),
+                                   (3, 4, 2, 700, 900, 64, False),
+                                   (1, 8, 8, 1536, 1536, 64, True)])
+def test_grid_modes_agree_bit_for_bit(shape):
+    """One CTA per work tile and the persistent grid (snake order) compute
+    identical outputs."""
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=43)
+    o1, l1 = _run(q, k, v, causal, grid_mode=1)
+    o2, l2 = _run(q, k, v, causal, grid_mode=2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
