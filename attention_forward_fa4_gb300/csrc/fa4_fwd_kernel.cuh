@@ -684,23 +684,26 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
       break;
     tc_fence_after_sync();
-    uint32_t x[D];
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) tmem_ld_x32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t x[32];
+      tmem_ld_x32(o_addr + c * 32, x);
+      tmem_wait_ld_x32(x);
+      if (c == D / 32 - 1) {
+        // O_t is read out: the next work tile's first P*V may overwrite it.
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::bOFree + t));
+      }
+      if (row_valid) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-    // O_t is in registers: the next work tile's first P*V may overwrite it.
-    tc_fence_before_sync();
-    mbar_arrive(bar(L::bOFree + t));
-    if (row_valid) {
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(x[8 * c + 0]) * inv_l, __uint_as_float(x[8 * c + 1]) * inv_l);
-        v.y = pack_bf16x2(__uint_as_float(x[8 * c + 2]) * inv_l, __uint_as_float(x[8 * c + 3]) * inv_l);
-        v.z = pack_bf16x2(__uint_as_float(x[8 * c + 4]) * inv_l, __uint_as_float(x[8 * c + 5]) * inv_l);
-        v.w = pack_bf16x2(__uint_as_float(x[8 * c + 6]) * inv_l, __uint_as_float(x[8 * c + 7]) * inv_l);
-        reinterpret_cast<uint4*>(orow)[c] = v;
+        for (int i = 0; i < 4; ++i) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(x[8 * i + 0]) * inv_l, __uint_as_float(x[8 * i + 1]) * inv_l);
+          v.y = pack_bf16x2(__uint_as_float(x[8 * i + 2]) * inv_l, __uint_as_float(x[8 * i + 3]) * inv_l);
+          v.z = pack_bf16x2(__uint_as_float(x[8 * i + 4]) * inv_l, __uint_as_float(x[8 * i + 5]) * inv_l);
+          v.w = pack_bf16x2(__uint_as_float(x[8 * i + 6]) * inv_l, __uint_as_float(x[8 * i + 7]) * inv_l);
+          reinterpret_cast<uint4*>(orow + c * 32)[i] = v;
+        }
       }
     }
   } else if (row_valid) {
@@ -769,18 +772,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // Register split: 256 softmax threads x 176 + 128 correction x 72 +
-  // 128 load/MMA x 88 = 65,536 = 512 threads x 128 at launch.
+  // Register split (setmaxnreg): 256 softmax threads, 128 correction, 128
+  // load/MMA; the total must equal the 512 x 128 the block launches with.
+  constexpr int kRegsSoftmax = 184;
+  constexpr int kRegsCorrection = D == 128 ? 56 : 64;
+  constexpr int kRegsLoadMma = D == 128 ? 88 : 80;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsCorrection + 128 * kRegsLoadMma == kThreads * 128,
+                "register split must use exactly the launch allocation");
   if (warp < 8) {
-    regs_increase<176>();
+    regs_increase<kRegsSoftmax>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
     softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, p, w);
   } else if (warp < 12) {
-    regs_decrease<72>();
+    regs_decrease<kRegsCorrection>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
     correction_role<D, CAUSAL>(sbase, smem, tmem, p, w);
   } else {
-    regs_decrease<88>();
+    regs_decrease<kRegsLoadMma>();
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
       load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, p, w);
