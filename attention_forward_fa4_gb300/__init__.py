@@ -51,13 +51,14 @@ class _Options(ctypes.Structure):
                 ("grid_mode", ctypes.c_int)]
 
 
-TRACE_EVENTS = 19
+TRACE_EVENTS = 21
 TRACE_STEPS = 128
 TRACE_EVENT_NAMES = ("mma_s_wait", "mma_s_issued", "mma_pv_wait", "mma_pv_issued",
                      "sm_s_ready", "sm_loaded", "sm_exp_done", "sm_arrived",
                      "co_wake", "co_arrived", "mma_s_go", "mma_pv_go", "sm_arrived_q1",
                      "sm_arrived_q2", "sm_arrived_q3", "sm_max_done",
-                     "mma_committed", "mma_v_ready", "load_issued")
+                     "mma_committed", "mma_v_ready", "load_issued", "sm_max_loop",
+                     "sm_c_done")
 
 
 def load_library():

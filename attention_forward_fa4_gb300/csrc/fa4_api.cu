@@ -13,6 +13,9 @@
 #include "fa4.h"
 #include "fa4_internal.h"
 
+static_assert(fa4::kTraceEvents == FA4_TRACE_EVENTS && fa4::kTraceSteps == FA4_TRACE_STEPS,
+              "trace layout differs between the kernel and the C header");
+
 namespace fa4 {
 namespace {
 
@@ -265,9 +268,9 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.strict_order = op.strict_mma_order ? 1 : 0;
 
   const int emu = op.exp2_emulation ? 8 : 0;
-  cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu,
+  cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu, persistent,
                                                static_cast<unsigned>(grid), s)
-                              : launch_fwd_d128(tq, tk, tv, p, causal != 0, emu,
+                              : launch_fwd_d128(tq, tk, tv, p, causal != 0, emu, persistent,
                                                 static_cast<unsigned>(grid), s);
   return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
 }

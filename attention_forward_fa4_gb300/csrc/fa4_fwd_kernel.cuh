@@ -16,7 +16,8 @@
 //               that need no rescale never wait for it
 
 //   warp 12     TMA load warp: Q once, then K_j / V_j into a ring of slots
-//   warp 13     MMA warp: one thread issues every tcgen05.mma
+//   warp 13     MMA warp: the whole warp runs the issue loop with uniform
+//               operands; one elected lane issues every tcgen05.mma
 //   warps 14-15 idle
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
@@ -111,7 +112,7 @@ enum TraceEvent : int {
   kTrMmaPvIssued,      // MMA: O_t += P_t V_j issued and committed
   kTrSmSReady,         // softmax: S_t visible (s_full passed)
   kTrSmLoaded,         // softmax: S row in registers
-  kTrSmExpDone,        // softmax: P computed and packed
+  kTrSmExpDone,        // softmax: P computed and packed (before the TMEM stores)
   kTrSmArrived,        // softmax: P stored, barrier arrived
   kTrCoWake,           // correction: p_full passed
   kTrCoArrived,        // correction: o_ready arrived
@@ -124,6 +125,8 @@ enum TraceEvent : int {
   kTrMmaCommitted,     // MMA: slot-release commits of key block j issued
   kTrMmaVReady,        // MMA: V_j in shared memory (before any P_t V_j)
   kTrLoadIssued,       // load warp: V_j copy issued (t = 0) / K_j copy issued (t = 1)
+  kTrSmMaxLoop,        // softmax: block max reduced (before the warp vote)
+  kTrSmCDone,          // softmax: the correction warps have taken the last step's flags
   kTraceEvents
 };
 
@@ -133,6 +136,11 @@ __device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, in
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
     p.trace[((static_cast<size_t>(blockIdx.x) * kTraceEvents + ev) * kTraceSteps + j) * 2 + t] = c;
   }
+}
+
+// As trace_mark, recorded by lane 0 of a warp whose lanes all run the role.
+__device__ __forceinline__ void trace_mark_lane0(const FwdParams& p, int ev, int j, int t, int iter = 0) {
+  if ((threadIdx.x & 31) == 0) trace_mark(p, ev, j, t, iter);
 }
 
 template <int D>
@@ -163,6 +171,7 @@ struct Smem {
   static constexpr int kMisc = kFlags + 8 * 4;           // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;           // slack for 1 KB alignment
+  static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
@@ -217,6 +226,17 @@ struct Waiter {
   __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, unsigned id) const {
     return mbar_try_wait(bar, parity) || slow(bar, parity, id, false);
   }
+  // Warp-wide forms for a role that a whole warp runs: every lane waits and
+  // the outcome is made uniform, so the warp stays converged for the
+  // elect.sync issues that follow.
+  __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, unsigned id) const {
+    const bool ok = mbar_try_wait(bar, parity) || slow(bar, parity, id, true);
+    return __all_sync(0xffffffffu, ok);
+  }
+  __device__ __forceinline__ bool drain_warp(uint32_t bar, uint32_t parity, unsigned id) const {
+    const bool ok = mbar_try_wait(bar, parity) || slow(bar, parity, id, false);
+    return __all_sync(0xffffffffu, ok);
+  }
 };
 
 // ------------------------------------------------------------ tile geometry
@@ -225,8 +245,13 @@ struct Waiter {
 // c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... Causal tiles are numbered heaviest
 // first, so the pairs a CTA takes from consecutive rounds add up to about
 // the same work on every CTA.
-__device__ __forceinline__ int tile_of(int k) {
+// Without PERSIST the grid has one CTA per work tile and each CTA takes
+// exactly its own tile (the loops below then run once, with every running
+// counter starting from zero).
+template <bool PERSIST>
+__device__ __forceinline__ int tile_of(int k, int n_tiles) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if constexpr (!PERSIST) return k == 0 ? c : n_tiles;
   return k * g + ((k & 1) ? (g - 1 - c) : c);
 }
 
@@ -277,7 +302,7 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p, int id) {
 // Q once per work tile (after the previous tile's S MMAs have released the
 // Q buffers), then K_j, V_j of every key block into the slot ring; the
 // ring's fill counter runs on across work tiles.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PERSIST>
 __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, uint32_t sbase,
                                           const FwdParams& p, const Waiter& w) {
@@ -287,7 +312,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
   int n_q = 0;      // Q copies issued so far
   bool ok = true;
   int iter = 0;
-  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
+  for (int id = tile_of<PERSIST>(0, p.n_tiles); ok && id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     if (tl.nkv_max == 0) continue;
     if (n_q > 0 && !(ok = w.wait(bar(L::bQEmpty), static_cast<uint32_t>(n_q - 1) & 1u, L::bQEmpty)))
@@ -332,13 +357,21 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // so the tensor core computes tile 1's work while tile 0's softmax runs and
 // the other way round. S_t(j+1) overwrites the TMEM columns that P_t(j)
 // occupies and is issued right behind the P*V that reads them: the MMAs of
-// one issuing thread run through the SM's tensor core in issue order. With
-// FwdParams::strict_order set, S_t(j+1) instead waits for the P*V's commit.
+// one issuing thread run through the SM's tensor core in issue order (the
+// warp stays converged, so elect.sync picks the same lane for every MMA and
+// commit). With FwdParams::strict_order set, S_t(j+1) instead waits for the
+// P*V's commit.
+//
+// Measured on GB300: with the softmax warps busy on every SMSP, a single
+// issuing lane whose descriptors live in per-thread registers kept a
+// 128 x 128 x 128 MMA group to about 1000 cycles (about 600 with the SM
+// otherwise idle); the whole warp computing the same uniform operands and
+// one elected lane issuing brought it to about 850.
 //
 // Phases run on across the CTA's work tiles: the ring position, the count
 // of P*V MMAs per query tile and the count of earlier tiles whose O_t the
 // epilogue has to read before the next tile's first P*V overwrites it.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PERSIST>
 __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const FwdParams& p,
                                          const Waiter& w) {
   using L = Smem<D>;
@@ -361,9 +394,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-      mma_ss_lohi(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
+      mma_ss_lohi_warp(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
     }
-    mma_commit(bar(L::bSFull + t));
+    mma_commit_warp(bar(L::bSFull + t));
   };
   // O_t (+)= P_t V; each slice of P is issued once the softmax warps have
   // stored it. `phase` counts this tile's earlier P*V MMAs. Returns false on
@@ -372,23 +405,23 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
-      if (!w.wait(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
+      if (!w.wait_warp(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
 #pragma unroll
       for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
         // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
         const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
-        mma_ts_lohi(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+        mma_ts_lohi_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
       }
     }
-    mma_commit(bar(L::bPvDone + t));
+    mma_commit_warp(bar(L::bPvDone + t));
     return true;
   };
   auto wait_slot = [&](int pos) -> bool {
     const int s = pos % L::kSlots;
-    const bool ok = w.wait(bar(L::bKvFull + s), static_cast<uint32_t>(pos / L::kSlots) & 1u,
+    const bool ok = w.wait_warp(bar(L::bKvFull + s), static_cast<uint32_t>(pos / L::kSlots) & 1u,
                            L::bKvFull + s);
     tc_fence_after_sync();
     return ok;
@@ -400,10 +433,10 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   int n_epi[2] = {0, 0};        // earlier work tiles whose O_t the epilogue reads
   bool ok = true;
   int iter = 0;
-  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
+  for (int id = tile_of<PERSIST>(0, p.n_tiles); ok && id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     if (tl.nkv_max == 0) continue;
-    if (!(ok = w.wait(bar(L::bQ), static_cast<uint32_t>(n_q) & 1u, L::bQ))) break;
+    if (!(ok = w.wait_warp(bar(L::bQ), static_cast<uint32_t>(n_q) & 1u, L::bQ))) break;
     tc_fence_after_sync();
     ++n_q;
     // S_0(0), S_1(0)
@@ -411,73 +444,73 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (tl.nkv[t] == 0) continue;
-      trace_mark(p, kTrMmaSGo, 0, t, iter);
+      trace_mark_lane0(p, kTrMmaSGo, 0, t, iter);
       issue_s(t, cons % L::kSlots);
-      trace_mark(p, kTrMmaSIssued, 0, t, iter);
+      trace_mark_lane0(p, kTrMmaSIssued, 0, t, iter);
     }
-    mma_commit(bar(L::bKvEmpty + cons % L::kSlots));
+    mma_commit_warp(bar(L::bKvEmpty + cons % L::kSlots));
     ++cons;
-    if (tl.nkv_max == 1) mma_commit(bar(L::bQEmpty));     // no further S of this tile
+    if (tl.nkv_max == 1) mma_commit_warp(bar(L::bQEmpty));     // no further S of this tile
     for (int j = 0; ok && j < tl.nkv_max; ++j) {
       const int vpos = cons, kpos = cons + 1;             // V_j, then K_{j+1}
       const bool next = j + 1 < tl.nkv_max;
       if (!(ok = wait_slot(vpos))) break;
-      trace_mark(p, kTrMmaVReady, j, 0, iter);
+      trace_mark_lane0(p, kTrMmaVReady, j, 0, iter);
       bool k_ready = false;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= tl.nkv[t]) continue;
-        trace_mark(p, kTrMmaPvWait, j, t, iter);
-        if (!(ok = w.wait(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
+        trace_mark_lane0(p, kTrMmaPvWait, j, t, iter);
+        if (!(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
           break;
         if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
-            !(ok = w.wait(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
+            !(ok = w.wait_warp(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
           break;
         tc_fence_after_sync();
-        trace_mark(p, kTrMmaPvGo, j, t, iter);
+        trace_mark_lane0(p, kTrMmaPvGo, j, t, iter);
         if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t]))) break;
         ++n_pv[t];
-        trace_mark(p, kTrMmaPvIssued, j, t, iter);
+        trace_mark_lane0(p, kTrMmaPvIssued, j, t, iter);
         if (j + 1 >= tl.nkv[t]) continue;
-        trace_mark(p, kTrMmaSWait, j + 1, t, iter);
+        trace_mark_lane0(p, kTrMmaSWait, j + 1, t, iter);
         if (!k_ready) {
           if (!(ok = wait_slot(kpos))) break;
           k_ready = true;
         }
         if (p.strict_order) {
-          if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_pv[t] - 1) & 1u,
+          if (!(ok = w.wait_warp(bar(L::bPvDone + t), static_cast<uint32_t>(n_pv[t] - 1) & 1u,
                             L::bPvDone + t)))
             break;
           tc_fence_after_sync();
         }
-        trace_mark(p, kTrMmaSGo, j + 1, t, iter);
+        trace_mark_lane0(p, kTrMmaSGo, j + 1, t, iter);
         issue_s(t, kpos % L::kSlots);
-        trace_mark(p, kTrMmaSIssued, j + 1, t, iter);
+        trace_mark_lane0(p, kTrMmaSIssued, j + 1, t, iter);
       }
       if (!ok) break;
-      mma_commit(bar(L::bKvEmpty + vpos % L::kSlots));
+      mma_commit_warp(bar(L::bKvEmpty + vpos % L::kSlots));
       ++cons;
       if (next) {
         // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
-        mma_commit(bar(L::bKvEmpty + kpos % L::kSlots));
+        mma_commit_warp(bar(L::bKvEmpty + kpos % L::kSlots));
         ++cons;
       }
       // The last S MMAs of this work tile are issued: once they complete the
       // Q buffers may take the next tile's queries.
-      if (j + 2 == tl.nkv_max) mma_commit(bar(L::bQEmpty));
-      trace_mark(p, kTrMmaCommitted, j, 0, iter);
+      if (j + 2 == tl.nkv_max) mma_commit_warp(bar(L::bQEmpty));
+      trace_mark_lane0(p, kTrMmaCommitted, j, 0, iter);
     }
 #pragma unroll
     for (int t = 0; t < 2; ++t)
       if (tl.nkv[t] > 0) ++n_epi[t];
   }
   // Every MMA issued above has completed once this commit arrives.
-  mma_commit(bar(L::bDrain));
-  w.drain(bar(L::bDrain), 0u, L::bDrain);
+  mma_commit_warp(bar(L::bDrain));
+  w.drain_warp(bar(L::bDrain), 0u, L::bDrain);
 }
 
 // ------------------------------------------------------------ correction WG
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PERSIST>
 __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                                 const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
@@ -491,7 +524,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
   int n_step[2] = {0, 0};       // softmax steps seen per query tile (all work tiles)
   int iter = 0;
-  for (int id = tile_of(0); id < p.n_tiles; id = tile_of(++iter)) {
+  for (int id = tile_of<PERSIST>(0, p.n_tiles); id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     for (int j = 0; j < tl.nkv_max; ++j) {
 #pragma unroll
@@ -546,7 +579,7 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
@@ -565,10 +598,10 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   int n_step = 0;               // steps of this query tile over all work tiles
   bool ok = true;
   int iter = 0;
-  for (int id = tile_of(0); ok && id < p.n_tiles; id = tile_of(++iter)) {
+  for (int id = tile_of<PERSIST>(0, p.n_tiles); ok && id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
   const Tile tl = make_tile<CAUSAL>(p, id);
   const int row = tl.q0 + t * kBM + r;          // query index
-  const int n = tl.nkv[t];
+  const int n = t == 0 ? tl.nkv[0] : tl.nkv[1];  // (a runtime index would put Tile in local memory)
   // Keys k < lim_row are visible to this row; lim_min is the tile's smallest.
   const int lim_row = CAUSAL ? max(0, min(p.Sk, row + shift + 1)) : p.Sk;
   const int row_min = tl.q0 + t * kBM;
@@ -611,12 +644,14 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       for (int i = 0; i < 4; ++i)
         mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
     const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
+    if (tracer) trace_mark(p, kTrSmMaxLoop, j, t, iter);
     // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
     // than tau, decided per warp so the correction stays warp-uniform.
     const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
     if (!FA4_CDONE_EARLY && n_step > 0 &&
         !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bCDone + t)))
       break;
+    if (tracer) trace_mark(p, kTrSmCDone, j, t, iter);
     if (tracer) trace_mark(p, kTrSmMaxDone, j, t, iter);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
@@ -653,6 +688,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
       pk[pi] = pack_bf16x2(pp.x, pp.y);
     }
+    if (tracer) trace_mark(p, kTrSmExpDone, j, t, iter);
     constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
@@ -667,7 +703,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
-    if (tracer) trace_mark(p, kTrSmExpDone, j, t, iter);
     if (tracer) trace_mark(p, kTrSmArrived, j, t, iter);
     if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
     ++n_step;
@@ -723,7 +758,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 }
 
 // ------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     fa4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -782,19 +817,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     regs_increase<kRegsSoftmax>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD>(warp >> 2, sbase, smem, tmem, p, w);
+    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD, PERSIST>(warp >> 2, sbase, smem, tmem, p, w);
   } else if (warp < 12) {
     regs_decrease<kRegsCorrection>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D, CAUSAL>(sbase, smem, tmem, p, w);
+    correction_role<D, CAUSAL, PERSIST>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<kRegsLoadMma>();
     if (warp == kWarpLoad && lane == 0) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, p, w);
-    } else if (warp == kWarpMma && lane == 0) {
+      load_role<D, CAUSAL, PERSIST>(&tm_q, &tm_k, &tm_v, sbase, p, w);
+    } else if (warp == kWarpMma) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D, CAUSAL>(sbase, tmem, p, w);
+      mma_role<D, CAUSAL, PERSIST>(sbase, tmem, p, w);
     }
   }
 

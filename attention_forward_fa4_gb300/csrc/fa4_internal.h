@@ -10,11 +10,13 @@ namespace fa4 {
 
 // Enqueue the forward kernel for head dim 64 / 128. `emu_period` is 0
 // (MUFU.EX2 only) or 8 (one entry in 8 through the software 2^x).
+// `persistent` picks the instantiation whose CTAs visit work tiles in turn
+// (grid <= SM count); otherwise the grid has one CTA per work tile.
 cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const FwdParams& p, bool causal, int emu_period, unsigned grid,
-                           cudaStream_t stream);
+                           const FwdParams& p, bool causal, int emu_period, bool persistent,
+                           unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& p, bool causal, int emu_period, unsigned grid,
-                            cudaStream_t stream);
+                            const FwdParams& p, bool causal, int emu_period, bool persistent,
+                            unsigned grid, cudaStream_t stream);
 
 }  // namespace fa4

@@ -99,7 +99,7 @@ typedef struct {
     int grid_mode;
 } fa4_fwd_options;
 
-#define FA4_TRACE_EVENTS 19
+#define FA4_TRACE_EVENTS 21
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 1, no counters, no trace,

@@ -97,3 +97,12 @@ def test_without_a_device_valid_calls_report_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _call(lib) in (fa4.FA4_ERR_CUDA, fa4.FA4_ERR_UNSUPPORTED)
+
+
+def test_trace_layout_matches_header():
+    import attention_forward_fa4_gb300 as fa4
+    hdr = open(os.path.join(ROOT, "include", "fa4.h")).read()
+    n_ev = int(re.search(r"#define FA4_TRACE_EVENTS (\d+)", hdr).group(1))
+    n_st = int(re.search(r"#define FA4_TRACE_STEPS (\d+)", hdr).group(1))
+    assert fa4.TRACE_EVENTS == n_ev == len(fa4.TRACE_EVENT_NAMES)
+    assert fa4.TRACE_STEPS == n_st
