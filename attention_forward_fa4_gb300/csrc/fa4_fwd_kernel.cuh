@@ -16,6 +16,7 @@
 //               that need no rescale never wait for it
 
 //   warp 12     TMA load warp: Q once, then K_j / V_j into a ring of slots
+//               (whole warp, one elected lane issues each copy)
 //   warp 13     MMA warp: the whole warp runs the issue loop with uniform
 //               operands; one elected lane issues every tcgen05.mma
 //   warps 14-15 idle
@@ -45,9 +46,6 @@
 //   FA4_P_SLICES     1: P is stored and released to P*V as one 128-key block;
 //                    2: in two 64-key halves so P*V starts on the first half
 //                    while the second is being exponentiated.
-//   FA4_CDONE_EARLY  1: the softmax checks that the correction warps read the
-//                    previous flags while its scores load from TMEM; 0: after
-//                    the block max.
 //   FA4_WAIT_SPIN    0: waits poll mbarrier.try_wait (the thread may be
 //                    suspended for a system-dependent time); 1: poll
 //                    mbarrier.test_wait (never suspended); 2: try_wait with a
@@ -55,9 +53,6 @@
 //                    256 or 1024 ns nanosleep back-off.
 #ifndef FA4_P_SLICES
 #define FA4_P_SLICES 1
-#endif
-#ifndef FA4_CDONE_EARLY
-#define FA4_CDONE_EARLY 0
 #endif
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
@@ -160,15 +155,17 @@ struct Smem {
   static constexpr int bPFull = bSFull + 2;              // [2]
   static constexpr int bOReady = bPFull + 2;             // [2]
   static constexpr int bPvDone = bOReady + 2;            // [2]
-  static constexpr int bCDone = bPvDone + 2;             // [2]
-  static constexpr int bPHalf = bCDone + 2;              // [2 tiles][2 halves]
+  static constexpr int bCDone = bPvDone + 2;             // [2 tiles][2 buffers]
+  static constexpr int bPHalf = bCDone + 4;              // [2 tiles][2 halves]
   static constexpr int bQEmpty = bPHalf + 4;             // Q tiles free for the next work tile
   static constexpr int bOFree = bQEmpty + 1;             // [2] epilogue has read O_t
   static constexpr int bDrain = bOFree + 2;
   static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kAlpha = kBars + kNumBars * 8;    // float [2][128]
-  static constexpr int kFlags = kAlpha + 2 * kBM * 4;    // int [2][4]
-  static constexpr int kMisc = kFlags + 8 * 4;           // tmem base, abort flag
+  // Rescale hand-off from softmax to correction, double-buffered by step
+  // parity: alpha float [2 buffers][2 tiles][128], flags int [2][2][4].
+  static constexpr int kAlpha = kBars + kNumBars * 8;
+  static constexpr int kFlags = kAlpha + 4 * kBM * 4;
+  static constexpr int kMisc = kFlags + 16 * 4;          // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;           // slack for 1 KB alignment
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
@@ -315,37 +312,37 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
   for (int id = tile_of<PERSIST>(0, p.n_tiles); ok && id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
     const Tile tl = make_tile<CAUSAL>(p, id);
     if (tl.nkv_max == 0) continue;
-    if (n_q > 0 && !(ok = w.wait(bar(L::bQEmpty), static_cast<uint32_t>(n_q - 1) & 1u, L::bQEmpty)))
+    if (n_q > 0 && !(ok = w.wait_warp(bar(L::bQEmpty), static_cast<uint32_t>(n_q - 1) & 1u, L::bQEmpty)))
       break;
-    mbar_arrive_expect_tx(bar(L::bQ), 2u * L::kTileBytes);
+    mbar_arrive_expect_tx_warp(bar(L::bQ), 2u * L::kTileBytes);
 #pragma unroll
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int pn = 0; pn < L::kPanels; ++pn)
-        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + pn * L::kPanelBytes, tm_q, bar(L::bQ),
+        tma_load_4d_warp(sbase + L::kQ + t * L::kTileBytes + pn * L::kPanelBytes, tm_q, bar(L::bQ),
                     pn * 64, tl.h, tl.q0 + t * kBM, tl.b);
     ++n_q;
     for (int idx = 0; idx < 2 * tl.nkv_max; ++idx) {   // K_0, V_0, K_1, V_1, ...
       const int s = fill % L::kSlots;
       const uint32_t n = static_cast<uint32_t>(fill / L::kSlots);
-      if (!(ok = w.wait(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s))) break;
-      mbar_arrive_expect_tx(bar(L::bKvFull + s), L::kTileBytes);
+      if (!(ok = w.wait_warp(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s))) break;
+      mbar_arrive_expect_tx_warp(bar(L::bKvFull + s), L::kTileBytes);
       const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
       const int row = (idx >> 1) * kBN;
 #pragma unroll
       for (int pn = 0; pn < L::kPanels; ++pn)
-        tma_load_4d(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm,
+        tma_load_4d_warp(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm,
                     bar(L::bKvFull + s), pn * 64, tl.hk, row, tl.b);
       ++fill;
-      trace_mark(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1, iter);
+      trace_mark_lane0(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1, iter);
     }
   }
-  if (!ok || *w.abort) {
+  if (__any_sync(0xffffffffu, !ok || *w.abort)) {
     // Let every copy this warp started land before the CTA frees its memory.
-    if (n_q > 0) w.drain(bar(L::bQ), static_cast<uint32_t>(n_q - 1) & 1u, L::bQ);
+    if (n_q > 0) w.drain_warp(bar(L::bQ), static_cast<uint32_t>(n_q - 1) & 1u, L::bQ);
     for (int idx = max(0, fill - L::kSlots); idx < fill; ++idx) {
       const int s = idx % L::kSlots;
-      w.drain(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u, L::bKvFull + s);
+      w.drain_warp(bar(L::bKvFull + s), static_cast<uint32_t>(idx / L::kSlots) & 1u, L::bKvFull + s);
     }
   }
 }
@@ -531,14 +528,16 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
       for (int t = 0; t < 2; ++t) {
         if (j >= tl.nkv[t]) continue;
         const int cnt = n_step[t]++;
+        const int buf = cnt & 1;
         if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
         tc_fence_after_sync();
         if (warp == 8 && lane == 0) trace_mark(p, kTrCoWake, j, t, iter);
-        const bool flagged = j > 0 && flags_s[t * 4 + wq] != 0;
-        const float a = flagged ? alpha_s[t * kBM + r] : 1.0f;
-        // flags and alpha of this step are read: the softmax may overwrite them
+        const bool flagged = j > 0 && flags_s[(buf * 2 + t) * 4 + wq] != 0;
+        const float a = flagged ? alpha_s[(buf * 2 + t) * kBM + r] : 1.0f;
+        // this buffer's flags and alpha are read: the softmax may reuse it
+        // two steps on
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bCDone + t));
+        if (lane == 0) mbar_arrive(bar(L::bCDone + 2 * t + buf));
         if (flagged) {
           // This 32-row group's reference max moved: O_t <- alpha * O_t once
           // the previous P*V into O_t has completed, then release the group.
@@ -619,11 +618,17 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    // The correction warps must have read the flags / alpha of step j-1
-    // before they are overwritten (normally long done).
-    if (FA4_CDONE_EARLY && n_step > 0 &&
-        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bCDone + t)))
-      break;
+    // This step's hand-off buffer was last used two steps ago; the
+    // correction warps must have read it (long done). The check overlaps
+    // the TMEM load for D = 128 and follows the block max for D = 64 (each
+    // placement measured the faster for its head dimension).
+    const int buf = n_step & 1;
+    auto wait_handoff = [&]() -> bool {
+      return n_step < 2 ||
+             w.wait(bar(L::bCDone + 2 * t + buf), static_cast<uint32_t>((n_step >> 1) - 1) & 1u,
+                    L::bCDone + 2 * t + buf);
+    };
+    if (D == 128 && !(ok = wait_handoff())) break;
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
@@ -648,22 +653,22 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
     // than tau, decided per warp so the correction stays warp-uniform.
     const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-    if (!FA4_CDONE_EARLY && n_step > 0 &&
-        !(ok = w.wait(bar(L::bCDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bCDone + t)))
-      break;
+    if (D != 128 && !(ok = wait_handoff())) break;
     if (tracer) trace_mark(p, kTrSmCDone, j, t, iter);
     if (tracer) trace_mark(p, kTrSmMaxDone, j, t, iter);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
       l *= alpha;
       if (m_cand != -INFINITY) m_ref = m_cand;
-      alpha_s[t * kBM + r] = alpha;
+      alpha_s[(buf * 2 + t) * kBM + r] = alpha;
       if (j > 0) ++n_rescaled;
     }
-    if (lane == 0) flags_s[t * 4 + wq] = warp_need ? 1 : 0;
+    if (lane == 0) flags_s[(buf * 2 + t) * 4 + wq] = warp_need ? 1 : 0;
     // Decision made: the correction warps may read flag / alpha and rescale
     // O_t while the exponentials run; row groups that need no rescale
-    // release O_t for the next P*V right away.
+    // release O_t for the next P*V right away. (Every thread arrives on
+    // p_full after its own alpha store; measured faster than one arrival
+    // per warp behind a warp barrier.)
     mbar_arrive(bar(L::bPFull + t));
     __syncwarp();
     if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
@@ -787,7 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bPFull + t), kBM);
       mbar_init(bar(L::bOReady + t), 4);
       mbar_init(bar(L::bPvDone + t), 1);
-      mbar_init(bar(L::bCDone + t), 4);
+      mbar_init(bar(L::bCDone + 2 * t), 4);
+      mbar_init(bar(L::bCDone + 2 * t + 1), 4);
       mbar_init(bar(L::bPHalf + 2 * t), 4);
       mbar_init(bar(L::bPHalf + 2 * t + 1), 4);
       mbar_init(bar(L::bOFree + t), kBM);
@@ -824,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     correction_role<D, CAUSAL, PERSIST>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<kRegsLoadMma>();
-    if (warp == kWarpLoad && lane == 0) {
+    if (warp == kWarpLoad) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
       load_role<D, CAUSAL, PERSIST>(&tm_q, &tm_k, &tm_v, sbase, p, w);
     } else if (warp == kWarpMma) {
