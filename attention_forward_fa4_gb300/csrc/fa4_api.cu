@@ -268,10 +268,10 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.strict_order = op.strict_mma_order ? 1 : 0;
 
   const int emu = op.exp2_emulation ? 8 : 0;
-  cudaError_t err = (d == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, emu, persistent,
-                                               static_cast<unsigned>(grid), s)
-                              : launch_fwd_d128(tq, tk, tv, p, causal != 0, emu, persistent,
-                                                static_cast<unsigned>(grid), s);
+  const bool traced = op.trace != nullptr;
+  auto launch = (d == 64) ? (traced ? launch_fwd_d64_traced : launch_fwd_d64)
+                          : (traced ? launch_fwd_d128_traced : launch_fwd_d128);
+  cudaError_t err = launch(tq, tk, tv, p, causal != 0, emu, persistent, static_cast<unsigned>(grid), s);
   return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
 }
 

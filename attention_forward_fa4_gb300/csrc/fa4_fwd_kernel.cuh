@@ -97,8 +97,10 @@ struct FwdParams {
 // first work tile:
 //   trace[((cta * kTraceEvents + event) * kTraceSteps + j) * 2 + t].
 // The MMA thread, lane 0 of the first softmax warp of each tile and lane 0
-// of the first correction warp record. A null pointer costs one uniform
-// branch per event.
+// of the first correction warp record. Only the kernels instantiated with
+// TRACE = true contain the marks (the host picks them when a trace buffer
+// is passed); in the others they compile to nothing, because even untaken
+// checks at every mark cost about 8 % of forward throughput.
 constexpr int kTraceSteps = 128;
 enum TraceEvent : int {
   kTrMmaSWait = 0,     // MMA: starts waiting for the S_t slot / K_j
@@ -125,7 +127,9 @@ enum TraceEvent : int {
   kTraceEvents
 };
 
+template <bool TRACE>
 __device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, int t, int iter = 0) {
+  if constexpr (!TRACE) return;
   if (p.trace != nullptr && iter == 0 && static_cast<int>(blockIdx.x) < p.trace_ctas && j < kTraceSteps) {
     uint64_t c;
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
@@ -134,8 +138,9 @@ __device__ __forceinline__ void trace_mark(const FwdParams& p, int ev, int j, in
 }
 
 // As trace_mark, recorded by lane 0 of a warp whose lanes all run the role.
+template <bool TRACE>
 __device__ __forceinline__ void trace_mark_lane0(const FwdParams& p, int ev, int j, int t, int iter = 0) {
-  if ((threadIdx.x & 31) == 0) trace_mark(p, ev, j, t, iter);
+  if ((threadIdx.x & 31) == 0) trace_mark<TRACE>(p, ev, j, t, iter);
 }
 
 template <int D>
@@ -299,7 +304,7 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p, int id) {
 // Q once per work tile (after the previous tile's S MMAs have released the
 // Q buffers), then K_j, V_j of every key block into the slot ring; the
 // ring's fill counter runs on across work tiles.
-template <int D, bool CAUSAL, bool PERSIST>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
 __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, uint32_t sbase,
                                           const FwdParams& p, const Waiter& w) {
@@ -334,7 +339,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
         tma_load_4d_warp(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm,
                     bar(L::bKvFull + s), pn * 64, tl.hk, row, tl.b);
       ++fill;
-      trace_mark_lane0(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1, iter);
+      trace_mark_lane0<TRACE>(p, kTrLoadIssued, idx >> 1, (idx & 1) ? 0 : 1, iter);
     }
   }
   if (__any_sync(0xffffffffu, !ok || *w.abort)) {
@@ -368,7 +373,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // Phases run on across the CTA's work tiles: the ring position, the count
 // of P*V MMAs per query tile and the count of earlier tiles whose O_t the
 // epilogue has to read before the next tile's first P*V overwrites it.
-template <int D, bool CAUSAL, bool PERSIST>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
 __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const FwdParams& p,
                                          const Waiter& w) {
   using L = Smem<D>;
@@ -441,9 +446,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (tl.nkv[t] == 0) continue;
-      trace_mark_lane0(p, kTrMmaSGo, 0, t, iter);
+      trace_mark_lane0<TRACE>(p, kTrMmaSGo, 0, t, iter);
       issue_s(t, cons % L::kSlots);
-      trace_mark_lane0(p, kTrMmaSIssued, 0, t, iter);
+      trace_mark_lane0<TRACE>(p, kTrMmaSIssued, 0, t, iter);
     }
     mma_commit_warp(bar(L::bKvEmpty + cons % L::kSlots));
     ++cons;
@@ -452,24 +457,24 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       const int vpos = cons, kpos = cons + 1;             // V_j, then K_{j+1}
       const bool next = j + 1 < tl.nkv_max;
       if (!(ok = wait_slot(vpos))) break;
-      trace_mark_lane0(p, kTrMmaVReady, j, 0, iter);
+      trace_mark_lane0<TRACE>(p, kTrMmaVReady, j, 0, iter);
       bool k_ready = false;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= tl.nkv[t]) continue;
-        trace_mark_lane0(p, kTrMmaPvWait, j, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaPvWait, j, t, iter);
         if (!(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
           break;
         if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
             !(ok = w.wait_warp(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
           break;
         tc_fence_after_sync();
-        trace_mark_lane0(p, kTrMmaPvGo, j, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaPvGo, j, t, iter);
         if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t]))) break;
         ++n_pv[t];
-        trace_mark_lane0(p, kTrMmaPvIssued, j, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaPvIssued, j, t, iter);
         if (j + 1 >= tl.nkv[t]) continue;
-        trace_mark_lane0(p, kTrMmaSWait, j + 1, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaSWait, j + 1, t, iter);
         if (!k_ready) {
           if (!(ok = wait_slot(kpos))) break;
           k_ready = true;
@@ -480,9 +485,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
             break;
           tc_fence_after_sync();
         }
-        trace_mark_lane0(p, kTrMmaSGo, j + 1, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaSGo, j + 1, t, iter);
         issue_s(t, kpos % L::kSlots);
-        trace_mark_lane0(p, kTrMmaSIssued, j + 1, t, iter);
+        trace_mark_lane0<TRACE>(p, kTrMmaSIssued, j + 1, t, iter);
       }
       if (!ok) break;
       mma_commit_warp(bar(L::bKvEmpty + vpos % L::kSlots));
@@ -495,7 +500,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       // The last S MMAs of this work tile are issued: once they complete the
       // Q buffers may take the next tile's queries.
       if (j + 2 == tl.nkv_max) mma_commit_warp(bar(L::bQEmpty));
-      trace_mark_lane0(p, kTrMmaCommitted, j, 0, iter);
+      trace_mark_lane0<TRACE>(p, kTrMmaCommitted, j, 0, iter);
     }
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -507,7 +512,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 }
 
 // ------------------------------------------------------------ correction WG
-template <int D, bool CAUSAL, bool PERSIST>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
 __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                                 const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
@@ -531,7 +536,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         const int buf = cnt & 1;
         if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
         tc_fence_after_sync();
-        if (warp == 8 && lane == 0) trace_mark(p, kTrCoWake, j, t, iter);
+        if (warp == 8 && lane == 0) trace_mark<TRACE>(p, kTrCoWake, j, t, iter);
         const bool flagged = j > 0 && flags_s[(buf * 2 + t) * 4 + wq] != 0;
         const float a = flagged ? alpha_s[(buf * 2 + t) * kBM + r] : 1.0f;
         // this buffer's flags and alpha are read: the softmax may reuse it
@@ -559,7 +564,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::bOReady + t));
         }
-        if (warp == 8 && lane == 0) trace_mark(p, kTrCoArrived, j, t, iter);
+        if (warp == 8 && lane == 0) trace_mark<TRACE>(p, kTrCoArrived, j, t, iter);
       }
     }
   }
@@ -578,7 +583,7 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const FwdParams& p, const Waiter& w) {
   using L = Smem<D>;
@@ -612,28 +617,20 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
     tc_fence_after_sync();
     const bool tracer = (wq == 0 && lane == 0);
-    if (tracer) trace_mark(p, kTrSmSReady, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmSReady, j, t, iter);
     uint32_t s[128];
     tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    // This step's hand-off buffer was last used two steps ago; the
-    // correction warps must have read it (long done). The check overlaps
-    // the TMEM load for D = 128 and follows the block max for D = 64 (each
-    // placement measured the faster for its head dimension).
+    // Hand-off buffer of this step (the one step n - 2 used; the end of
+    // step n - 1 checked that the correction warps have read it).
     const int buf = n_step & 1;
-    auto wait_handoff = [&]() -> bool {
-      return n_step < 2 ||
-             w.wait(bar(L::bCDone + 2 * t + buf), static_cast<uint32_t>((n_step >> 1) - 1) & 1u,
-                    L::bCDone + 2 * t + buf);
-    };
-    if (D == 128 && !(ok = wait_handoff())) break;
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    if (tracer) trace_mark(p, kTrSmLoaded, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmLoaded, j, t, iter);
     if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
       const int lim = lim_row - j * kBN;                 // this row's first masked column
 #pragma unroll
@@ -649,13 +646,12 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       for (int i = 0; i < 4; ++i)
         mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
     const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
-    if (tracer) trace_mark(p, kTrSmMaxLoop, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmMaxLoop, j, t, iter);
     // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
     // than tau, decided per warp so the correction stays warp-uniform.
     const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-    if (D != 128 && !(ok = wait_handoff())) break;
-    if (tracer) trace_mark(p, kTrSmCDone, j, t, iter);
-    if (tracer) trace_mark(p, kTrSmMaxDone, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmCDone, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmMaxDone, j, t, iter);
     if (warp_need) {
       const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
       l *= alpha;
@@ -693,7 +689,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
       pk[pi] = pack_bf16x2(pp.x, pp.y);
     }
-    if (tracer) trace_mark(p, kTrSmExpDone, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
     constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
 #pragma unroll
     for (int half = 0; half < FA4_P_SLICES; ++half) {
@@ -708,8 +704,15 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     }
     const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
-    if (tracer) trace_mark(p, kTrSmArrived, j, t, iter);
-    if (lane == 0 && wq > 0) trace_mark(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
+    if (tracer) trace_mark<TRACE>(p, kTrSmArrived, j, t, iter);
+    if (lane == 0 && wq > 0) trace_mark<TRACE>(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
+    // The next step reuses the buffer of step n_step - 1: the correction
+    // warps must have read it. Checked here, where the warp would otherwise
+    // only wait for the next S, rather than on the next step's path.
+    if (n_step >= 1 &&
+        !(ok = w.wait(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
+                      L::bCDone + 2 * t + (buf ^ 1))))
+      break;
     ++n_step;
   }
 
@@ -763,7 +766,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 }
 
 // ------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -823,19 +826,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     regs_increase<kRegsSoftmax>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD, PERSIST>(warp >> 2, sbase, smem, tmem, p, w);
+    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD, PERSIST, TRACE>(warp >> 2, sbase, smem, tmem, p, w);
   } else if (warp < 12) {
     regs_decrease<kRegsCorrection>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D, CAUSAL, PERSIST>(sbase, smem, tmem, p, w);
+    correction_role<D, CAUSAL, PERSIST, TRACE>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<kRegsLoadMma>();
     if (warp == kWarpLoad) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      load_role<D, CAUSAL, PERSIST>(&tm_q, &tm_k, &tm_v, sbase, p, w);
+      load_role<D, CAUSAL, PERSIST, TRACE>(&tm_q, &tm_k, &tm_v, sbase, p, w);
     } else if (warp == kWarpMma) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D, CAUSAL, PERSIST>(sbase, tmem, p, w);
+      mma_role<D, CAUSAL, PERSIST, TRACE>(sbase, tmem, p, w);
     }
   }
 

@@ -9,14 +9,18 @@
 namespace fa4 {
 
 // Enqueue the forward kernel for head dim 64 / 128. `emu_period` is 0
-// (MUFU.EX2 only) or 8 (one entry in 8 through the software 2^x).
+// (MUFU.EX2 only) or 8 (one entry pair in 8 through the software 2^x).
 // `persistent` picks the instantiation whose CTAs visit work tiles in turn
-// (grid <= SM count); otherwise the grid has one CTA per work tile.
-cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const FwdParams& p, bool causal, int emu_period, bool persistent,
-                           unsigned grid, cudaStream_t stream);
-cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& p, bool causal, int emu_period, bool persistent,
-                            unsigned grid, cudaStream_t stream);
+// (grid <= SM count); otherwise the grid has one CTA per work tile. The
+// _traced forms record the cycle trace (FwdParams::trace).
+#define FA4_DECLARE_LAUNCH(name)                                                              \
+  cudaError_t name(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,         \
+                   const FwdParams& p, bool causal, int emu_period, bool persistent, unsigned grid, \
+                   cudaStream_t stream);
+FA4_DECLARE_LAUNCH(launch_fwd_d64)
+FA4_DECLARE_LAUNCH(launch_fwd_d128)
+FA4_DECLARE_LAUNCH(launch_fwd_d64_traced)
+FA4_DECLARE_LAUNCH(launch_fwd_d128_traced)
+#undef FA4_DECLARE_LAUNCH
 
 }  // namespace fa4

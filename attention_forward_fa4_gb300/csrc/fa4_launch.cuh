@@ -1,0 +1,38 @@
+// fa4_launch.cuh -- host-side launch of one forward kernel instantiation.
+// Included by the per-head-dimension translation units, which instantiate
+// it for their head dimension with trace marks compiled in or out.
+#pragma once
+#include "fa4_internal.h"
+
+namespace fa4 {
+namespace detail {
+
+template <int D, bool CAUSAL, int EMU, bool PERSIST, bool TRACE>
+cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, unsigned grid, cudaStream_t stream) {
+  constexpr int kSmem = Smem<D>::kAlloc;
+  auto kernel = fa4_fwd_kernel<D, CAUSAL, EMU, PERSIST, TRACE>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+// causal / non-causal x MUFU-only / one entry pair in 8 through the
+// software 2^x x one CTA per work tile / persistent grid.
+template <int D, bool TRACE>
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, bool causal, int emu_period, bool persistent,
+                       unsigned grid, cudaStream_t stream) {
+#define FA4_LAUNCH(C, E, P) launch_one<D, C, E, P, TRACE>(tq, tk, tv, p, grid, stream)
+  if (causal) {
+    if (emu_period) return persistent ? FA4_LAUNCH(true, 8, true) : FA4_LAUNCH(true, 8, false);
+    return persistent ? FA4_LAUNCH(true, 0, true) : FA4_LAUNCH(true, 0, false);
+  }
+  if (emu_period) return persistent ? FA4_LAUNCH(false, 8, true) : FA4_LAUNCH(false, 8, false);
+  return persistent ? FA4_LAUNCH(false, 0, true) : FA4_LAUNCH(false, 0, false);
+#undef FA4_LAUNCH
+}
+
+}  // namespace detail
+}  // namespace fa4
