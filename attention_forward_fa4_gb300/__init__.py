@@ -110,7 +110,7 @@ def _check(code: int, what: str) -> None:
 
 def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
-             tau: float = 8.0, exp2_emulation: bool = True,
+             tau: float = 8.0, exp2_emulation: int = 0,
              rescale_stats: Optional[torch.Tensor] = None,
              trace: Optional[torch.Tensor] = None, strict_mma_order: bool = False,
              grid_mode: int = 0, stream: Optional[torch.cuda.Stream] = None) -> None:
@@ -140,7 +140,11 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     opt = _Options()
     lib.fa4_fwd_default_options(ctypes.byref(opt))
     opt.tau = float(tau)
-    opt.exp2_emulation = 1 if exp2_emulation else 0
+    # True / False are accepted as 8 / 0 (one entry pair in 8 / none)
+    emu = 8 if exp2_emulation is True else int(exp2_emulation)
+    if emu not in (0, 4, 8):
+        raise ValueError("exp2_emulation must be 0, 4 or 8 (or a bool)")
+    opt.exp2_emulation = emu
     opt.strict_mma_order = 1 if strict_mma_order else 0
     opt.grid_mode = int(grid_mode)
     if rescale_stats is not None:

@@ -141,7 +141,7 @@ extern "C" {
 void fa4_fwd_default_options(fa4_fwd_options* opt) {
   if (!opt) return;
   opt->tau = 8.0f;
-  opt->exp2_emulation = 1;
+  opt->exp2_emulation = 0;
   opt->rescale_stats = nullptr;
   opt->trace = nullptr;
   opt->trace_ctas = 0;
@@ -177,7 +177,9 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (causal != 0 && causal != 1) return FA4_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return FA4_ERR_INVALID_ARG;
   if (!std::isfinite(op.tau) || op.tau < 0.0f || op.tau > 64.0f) return FA4_ERR_INVALID_ARG;
-  if (op.exp2_emulation != 0 && op.exp2_emulation != 1) return FA4_ERR_INVALID_ARG;
+  if (op.exp2_emulation != 0 && op.exp2_emulation != 1 && op.exp2_emulation != 4 &&
+      op.exp2_emulation != 8)
+    return FA4_ERR_INVALID_ARG;
   if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
   if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
@@ -267,7 +269,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.trace_ctas = op.trace ? op.trace_ctas : 0;
   p.strict_order = op.strict_mma_order ? 1 : 0;
 
-  const int emu = op.exp2_emulation ? 8 : 0;
+  const int emu = op.exp2_emulation == 1 ? 8 : op.exp2_emulation;   // pair period, 0 = off
   const bool traced = op.trace != nullptr;
   auto launch = (d == 64) ? (traced ? launch_fwd_d64_traced : launch_fwd_d64)
                           : (traced ? launch_fwd_d128_traced : launch_fwd_d128);

@@ -9,7 +9,8 @@
 namespace fa4 {
 
 // Enqueue the forward kernel for head dim 64 / 128. `emu_period` is 0
-// (MUFU.EX2 only) or 8 (one entry pair in 8 through the software 2^x).
+// (MUFU.EX2 only), 8 or 4 (one entry pair in 8 / in 4 through the
+// software 2^x).
 // `persistent` picks the instantiation whose CTAs visit work tiles in turn
 // (grid <= SM count); otherwise the grid has one CTA per work tile. The
 // _traced forms record the cycle trace (FwdParams::trace).

@@ -18,19 +18,23 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   return cudaGetLastError();
 }
 
-// causal / non-causal x MUFU-only / one entry pair in 8 through the
-// software 2^x x one CTA per work tile / persistent grid.
+// causal / non-causal x MUFU-only / one entry pair in 8 or in 4 through
+// the software 2^x x one CTA per work tile / persistent grid.
 template <int D, bool TRACE>
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, bool causal, int emu_period, bool persistent,
                        unsigned grid, cudaStream_t stream) {
-#define FA4_LAUNCH(C, E, P) launch_one<D, C, E, P, TRACE>(tq, tk, tv, p, grid, stream)
+#define FA4_LAUNCH(C, E) \
+  (persistent ? launch_one<D, C, E, true, TRACE>(tq, tk, tv, p, grid, stream) \
+              : launch_one<D, C, E, false, TRACE>(tq, tk, tv, p, grid, stream))
   if (causal) {
-    if (emu_period) return persistent ? FA4_LAUNCH(true, 8, true) : FA4_LAUNCH(true, 8, false);
-    return persistent ? FA4_LAUNCH(true, 0, true) : FA4_LAUNCH(true, 0, false);
+    if (emu_period == 8) return FA4_LAUNCH(true, 8);
+    if (emu_period == 4) return FA4_LAUNCH(true, 4);
+    return FA4_LAUNCH(true, 0);
   }
-  if (emu_period) return persistent ? FA4_LAUNCH(false, 8, true) : FA4_LAUNCH(false, 8, false);
-  return persistent ? FA4_LAUNCH(false, 0, true) : FA4_LAUNCH(false, 0, false);
+  if (emu_period == 8) return FA4_LAUNCH(false, 8);
+  if (emu_period == 4) return FA4_LAUNCH(false, 4);
+  return FA4_LAUNCH(false, 0);
 #undef FA4_LAUNCH
 }
 

@@ -1,7 +1,7 @@
 """Benchmark of the GB300 attention forward (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--tau T] [--no-emu]
+                    [--workload NAME] [--tau T] [--exp2-emulation 0|4|8]
 
 One step = one attention forward over the workload's synthetic BF16 input
 (default: B=2, Hq=Hkv=16, Sq=Sk=8192, d=128, causal). ``value`` is the
@@ -255,7 +255,7 @@ def run_ours(args, w: workloads.Workload) -> None:
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    kw = dict(tau=args.tau, exp2_emulation=not args.no_emu)
+    kw = dict(tau=args.tau, exp2_emulation=args.exp2_emulation)
 
     def launch():
         fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
@@ -345,7 +345,7 @@ def run_ours(args, w: workloads.Workload) -> None:
             "data": "synthetic",
             "config": dict(w.describe(), global_batch=w.B * world, parallelism=f"replica-shards{world}",
                            l2="flushed before every timed launch (256 MiB write)",
-                           tau=args.tau, exp2_emulation=not args.no_emu),
+                           tau=args.tau, exp2_emulation=args.exp2_emulation),
             "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
@@ -374,7 +374,8 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--workload", default=workloads.LONG_CAUSAL.name,
                     choices=[x.name for x in workloads.ALL_NAMED])
     ap.add_argument("--tau", type=float, default=8.0)
-    ap.add_argument("--no-emu", action="store_true")
+    ap.add_argument("--exp2-emulation", type=int, choices=[0, 4, 8], default=0,
+                    help="one softmax entry pair in N through the software 2^x (0: none)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -60,9 +60,12 @@ typedef struct {
      * 8.0 (= log2 256) is the default; 0.0 gives the eager online softmax.
      * Must be finite and in [0, 64]. */
     float tau;
-    /* Software 2^x beside MUFU.EX2 ("FlashAttention-4", §3.1.3): 1 runs a
-     * Cody-Waite + degree-3 Horner polynomial on 1/8 of the softmax entries,
-     * 0 sends every entry through MUFU.EX2. */
+    /* Software 2^x beside MUFU.EX2 ("FlashAttention-4", §3.1.3): N = 8 or
+     * N = 4 runs a Cody-Waite + degree-3 Horner polynomial on one softmax
+     * entry pair in N (12.5 % or 25 % of the entries; 1 means 8), 0 sends
+     * every entry through MUFU.EX2. Default 0: on GB300, whose MUFU issues
+     * twice the exponentials per clock of the B200 the method was tuned
+     * for, the all-MUFU path measured faster at both head dimensions. */
     int exp2_emulation;
     /* Optional DEVICE pointer to two uint64 counters, or NULL. When set, the
      * kernel adds [0] += number of (32-row group, key block) steps that
@@ -102,7 +105,7 @@ typedef struct {
 #define FA4_TRACE_EVENTS 21
 #define FA4_TRACE_STEPS 128
 
-/* Default options: tau = 8, exp2_emulation = 1, no counters, no trace,
+/* Default options: tau = 8, exp2_emulation = 0, no counters, no trace,
  * strict_mma_order = 0, grid_mode = 0. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 

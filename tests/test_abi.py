@@ -80,7 +80,7 @@ def test_options_are_validated(lib):
     from attention_forward_fa4_gb300 import _Options
     opt = _Options()
     lib.fa4_fwd_default_options(ctypes.byref(opt))
-    assert opt.tau == 8.0 and opt.exp2_emulation == 1 and not opt.rescale_stats
+    assert opt.tau == 8.0 and opt.exp2_emulation == 0 and not opt.rescale_stats
     for tau in (-1.0, float("inf"), 100.0):
         opt.tau = tau
         assert lib.fa4_fwd_ex(Q, K, V, O, L, 1, 2, 2, 64, 64, 64, 0.125, 0, ctypes.byref(opt),

@@ -60,7 +60,7 @@ EDGE_CASES = [
 
 
 @pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: "x".join(map(str, c)))
-@pytest.mark.parametrize("emu", [True, False], ids=["emu", "mufu"])
+@pytest.mark.parametrize("emu", [0, 8, 4], ids=["mufu", "emu8", "emu4"])
 def test_small_shapes_match_oracle(case, emu):
     B, Hq, Hkv, Sq, Sk, d, causal = case
     q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=31)
