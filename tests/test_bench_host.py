@@ -11,12 +11,15 @@ import torch.multiprocessing as mp
 
 import bench
 import workloads
+from tests import golden
 
 
 def test_table1_roofline_cycles_at_b200_constants():
-    # M = 256, N = d = 128 on B200: MMA ~2048, exp ~2048, SMEM ~1536 cycles.
-    c = bench.table1_cycles(256, 128, 128)
-    assert c == {"mma": 2048.0, "exp": 2048.0, "smem": 1536.0}
+    # The pages' printed cycle counts (tests/golden, with the citation).
+    t = golden.load("table1_forward_roofline_b200.txt")
+    c = bench.table1_cycles(int(t["M"]), int(t["N"]), int(t["d"]), flops_per_clk=t["flops_per_clk"],
+                            exp_per_clk=t["exp_per_clk"], smem_bytes_per_clk=t["smem_bytes_per_clk"])
+    assert c == {"mma": t["mma"], "exp": t["exp"], "smem": t["smem"]}
     # GB300 doubles MUFU throughput: exp halves, MMA and SMEM unchanged.
     g = bench.table1_cycles(256, 128, 128, exp_per_clk=32.0)
     assert g["exp"] == 1024.0 and g["mma"] == 2048.0
