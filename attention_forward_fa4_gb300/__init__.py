@@ -76,6 +76,11 @@ def load_library():
     lib.fa4_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                ctypes.POINTER(_Options), vp]
     lib.fa4_fwd_ex.restype = i32
+    lib.fa4_fwd_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.fa4_fwd_splitkv_workspace_bytes.restype = ctypes.c_uint64
+    lib.fa4_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                    i32, vp, ctypes.c_uint64, ctypes.POINTER(_Options), vp]
+    lib.fa4_fwd_splitkv.restype = i32
     lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa4_fwd_default_options.restype = None
     lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
@@ -113,11 +118,16 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              tau: float = 8.0, exp2_emulation: int = 0,
              rescale_stats: Optional[torch.Tensor] = None,
              trace: Optional[torch.Tensor] = None, strict_mma_order: bool = False,
-             grid_mode: int = 0, stream: Optional[torch.cuda.Stream] = None) -> None:
+             grid_mode: int = 0, num_splits: int = 0,
+             workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> None:
     """Write attention forward into preallocated ``o`` and ``lse``.
 
     Shapes: q, o [B,Sq,Hq,d]; k, v [B,Sk,Hkv,d] (BF16, contiguous, CUDA);
-    lse [B,Hq,Sq] fp32. ``scale`` defaults to 1/sqrt(d).
+    lse [B,Hq,Sq] fp32. ``scale`` defaults to 1/sqrt(d). ``num_splits`` > 0
+    runs the key-range split forward (``fa4_fwd_splitkv``) with
+    ``workspace`` (a CUDA uint8 tensor of at least
+    ``splitkv_workspace_bytes(...)`` bytes; allocated here when omitted).
     """
     lib = load_library()
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
@@ -158,10 +168,27 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                              f"{per_cta} elements")
         opt.trace = trace.data_ptr()
         opt.trace_ctas = trace.numel() // per_cta
+    if num_splits:
+        need = splitkv_workspace_bytes(B, Hq, Sq, d, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+        code = lib.fa4_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale),
+                                   int(bool(causal)), int(num_splits), workspace.data_ptr(),
+                                   workspace.numel(), ctypes.byref(opt), _stream_handle(stream))
+        _check(code, "fa4_fwd_splitkv")
+        return
     code = lib.fa4_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
                           ctypes.byref(opt), _stream_handle(stream))
     _check(code, "fa4_fwd_ex")
+
+
+def splitkv_workspace_bytes(B: int, Hq: int, Sq: int, d: int, num_splits: int) -> int:
+    """Device scratch bytes the key-range split forward needs."""
+    return int(load_library().fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits))
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,

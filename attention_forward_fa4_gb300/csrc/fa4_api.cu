@@ -163,9 +163,15 @@ const char* fa4_status_string(fa4_status s) {
 
 int fa4_version(void) { return 100; }
 
-fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                      int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
-                      const fa4_fwd_options* opt, fa4_stream_t stream) {
+namespace {
+
+// Shared body of fa4_fwd_ex and fa4_fwd_splitkv. With num_splits > 0 the
+// forward runs per key-range split into the workspace and a merge kernel
+// writes o / lse; num_splits == 0 is the plain forward.
+fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                    int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                    const fa4_fwd_options* opt, int num_splits, void* workspace,
+                    size_t workspace_bytes, fa4_stream_t stream) {
   using namespace fa4;
   fa4_fwd_options o_def;
   fa4_fwd_default_options(&o_def);
@@ -183,6 +189,7 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
   if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0) return FA4_OK;  // empty output: nothing to do
   if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
   auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -201,8 +208,27 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
       overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
       overlaps(lse, lse_bytes, v, kv_bytes))
     return FA4_ERR_INVALID_ARG;
+  // Key-range split: split_blocks key blocks per split; splits that would
+  // start past the last key block are dropped.
+  const int nblk_all = (Sk + kBN - 1) / kBN;
+  int n_splits = 1, split_blocks = nblk_all > 0 ? nblk_all : 1;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (num_splits > 0 && Sk > 0) {
+    const uint64_t need = fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits);
+    if (!workspace || workspace_bytes < need) return FA4_ERR_INVALID_ARG;
+    if (mis16(workspace)) return FA4_ERR_MISALIGNED;
+    if (overlaps(workspace, need, q, q_bytes) || overlaps(workspace, need, k, kv_bytes) ||
+        overlaps(workspace, need, v, kv_bytes) || overlaps(workspace, need, o, q_bytes) ||
+        overlaps(workspace, need, lse, lse_bytes))
+      return FA4_ERR_INVALID_ARG;
+    split_blocks = (nblk_all + num_splits - 1) / num_splits;
+    n_splits = (nblk_all + split_blocks - 1) / split_blocks;
+    o_part = static_cast<float*>(workspace);
+    lse_part = o_part + static_cast<uint64_t>(num_splits) * B * Sq * Hq * d;
+  }
   const int64_t n_qblk = (static_cast<int64_t>(Sq) + 2 * kBM - 1) / (2 * kBM);
-  const int64_t n_tiles = n_qblk * B * Hq;
+  const int64_t n_tiles = n_qblk * B * Hq * n_splits;
   if (n_tiles > 0x7fffffffLL) return FA4_ERR_UNSUPPORTED;
   // TMA limits: every global stride below 2^40 bytes.
   if (static_cast<uint64_t>(Sq) * Hq * d * 2 >= (1ull << 40) ||
@@ -268,13 +294,46 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   p.trace = op.trace;
   p.trace_ctas = op.trace ? op.trace_ctas : 0;
   p.strict_order = op.strict_mma_order ? 1 : 0;
+  p.n_splits = n_splits;
+  p.split_blocks = split_blocks;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
 
   const int emu = op.exp2_emulation == 1 ? 8 : op.exp2_emulation;   // pair period, 0 = off
   const bool traced = op.trace != nullptr;
   auto launch = (d == 64) ? (traced ? launch_fwd_d64_traced : launch_fwd_d64)
                           : (traced ? launch_fwd_d128_traced : launch_fwd_d128);
   cudaError_t err = launch(tq, tk, tv, p, causal != 0, emu, persistent, static_cast<unsigned>(grid), s);
-  return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
+  if (err != cudaSuccess) return FA4_ERR_CUDA;
+  if (o_part) {
+    err = launch_merge_splits(o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, n_splits, B,
+                              Sq, Hq, d, s);
+    if (err != cudaSuccess) return FA4_ERR_CUDA;
+  }
+  return FA4_OK;
+}
+
+}  // namespace
+
+fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                      const fa4_fwd_options* opt, fa4_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr, 0, stream);
+}
+
+uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_splits) {
+  if (B < 0 || Hq < 0 || Sq < 0 || d < 0 || num_splits < 0) return 0;
+  const uint64_t rows = static_cast<uint64_t>(num_splits) * B * Sq * Hq;
+  return rows * static_cast<uint64_t>(d) * 4 + rows * 4;
+}
+
+fa4_status fa4_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                           int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                           int num_splits, void* workspace, uint64_t workspace_bytes,
+                           const fa4_fwd_options* opt, fa4_stream_t stream) {
+  if (num_splits < 1) return FA4_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, num_splits, workspace,
+                  static_cast<size_t>(workspace_bytes), stream);
 }
 
 fa4_status fa4_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

@@ -87,7 +87,16 @@ struct FwdParams {
   unsigned long long* trace;   // optional per-role cycle trace (see trace_mark)
   int trace_ctas;              // CTAs (by blockIdx.x) that record a trace
   int strict_order;            // 1: S_t(j+1) waits for P_t(j) V_j to complete
-  int n_tiles;                 // n_qblk * B * Hq work tiles, visited by a persistent grid
+  int n_tiles;                 // n_qblk * B * Hq * n_splits work tiles
+  // Key-range split: work tile id = (query tile pair) * n_splits + split;
+  // split s covers key blocks [s * split_blocks, (s + 1) * split_blocks).
+  // With o_part set, each split writes its normalised partial output
+  // o_part[s][B][Sq][Hq][D] and lse_part[s][B][Hq][Sq] (fp32) instead of
+  // o / lse; a merge kernel combines them.
+  int n_splits;
+  int split_blocks;
+  float* o_part;
+  float* lse_part;
 };
 
 // ------------------------------------------------------------ cycle trace
@@ -259,13 +268,18 @@ __device__ __forceinline__ int tile_of(int k, int n_tiles) {
 
 struct Tile {
   int b, h, hk, q0;
-  int nkv[2];       // key blocks each query tile visits
+  int split;        // key-range split of this work tile
+  int kv0;          // first key block of the split
+  int nkv[2];       // key blocks each query tile visits (within the split)
   int nkv_max;
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ Tile make_tile(const FwdParams& p, int id) {
+__device__ __forceinline__ Tile make_tile(const FwdParams& p, int id_split) {
   Tile tl;
+  const int id = id_split / p.n_splits;
+  tl.split = id_split - id * p.n_splits;
+  tl.kv0 = tl.split * p.split_blocks;
   const int n_bh = p.B * p.Hq;
   const int per_chunk = p.head_chunk * p.n_qblk;
   const int chunk = id / per_chunk;
@@ -294,6 +308,7 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p, int id) {
         n = nblk;
       }
     }
+    n = max(0, min(n - tl.kv0, p.split_blocks));   // the split's share
     tl.nkv[t] = n;
     tl.nkv_max = max(tl.nkv_max, n);
   }
@@ -333,7 +348,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
       if (!(ok = w.wait_warp(bar(L::bKvEmpty + s), (n & 1u) ^ 1u, L::bKvEmpty + s))) break;
       mbar_arrive_expect_tx_warp(bar(L::bKvFull + s), L::kTileBytes);
       const CUtensorMap* tm = (idx & 1) ? tm_v : tm_k;
-      const int row = (idx >> 1) * kBN;
+      const int row = (tl.kv0 + (idx >> 1)) * kBN;
 #pragma unroll
       for (int pn = 0; pn < L::kPanels; ++pn)
         tma_load_4d_warp(sbase + L::kRing + s * L::kTileBytes + pn * L::kPanelBytes, tm,
@@ -631,8 +646,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     if (tracer) trace_mark<TRACE>(p, kTrSmLoaded, j, t, iter);
-    if ((j + 1) * kBN > lim_min) {     // tile-uniform: this block has masked keys
-      const int lim = lim_row - j * kBN;                 // this row's first masked column
+    const int kb = tl.kv0 + j;           // absolute key block
+    if ((kb + 1) * kBN > lim_min) {      // tile-uniform: this block has masked keys
+      const int lim = lim_row - kb * kBN;                // this row's first masked column
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
     }
@@ -717,12 +733,17 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   }
 
   if (!ok) break;
-  // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l)
+  // ---- epilogue: O / l -> BF16 -> global, LSE = ln2 * (m_ref + log2 l);
+  // with a key-range split, fp32 O / l and LSE of this split into the
+  // partial buffers instead.
   const bool row_valid = row < p.Sq;
   const bool has_keys = n > 0 && m_ref != -INFINITY;
   const float inv_l = has_keys ? 1.0f / l : 0.0f;
-  __nv_bfloat16* orow =
-      p.o + ((static_cast<int64_t>(tl.b) * p.Sq + row) * p.Hq + tl.h) * static_cast<int64_t>(D);
+  const bool partial = p.o_part != nullptr;
+  const int64_t orow_idx = (static_cast<int64_t>(tl.b) * p.Sq + row) * p.Hq + tl.h;
+  const int64_t part_off = static_cast<int64_t>(tl.split) * p.B * p.Sq * p.Hq;
+  __nv_bfloat16* orow = p.o + orow_idx * static_cast<int64_t>(D);
+  float* prow = p.o_part + (part_off + orow_idx) * static_cast<int64_t>(D);
   if (n > 0) {
     if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
       break;
@@ -737,7 +758,13 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
         tc_fence_before_sync();
         mbar_arrive(bar(L::bOFree + t));
       }
-      if (row_valid) {
+      if (row_valid && partial) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(prow + c * 32)[i] =
+              make_float4(__uint_as_float(x[4 * i + 0]) * inv_l, __uint_as_float(x[4 * i + 1]) * inv_l,
+                          __uint_as_float(x[4 * i + 2]) * inv_l, __uint_as_float(x[4 * i + 3]) * inv_l);
+      } else if (row_valid) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 v;
@@ -749,14 +776,22 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
         }
       }
     }
+  } else if (row_valid && partial) {
+    float4* dst = reinterpret_cast<float4*>(prow);
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   } else if (row_valid) {
     uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   if (row_valid) {
-    p.lse[(static_cast<int64_t>(tl.b) * p.Hq + tl.h) * p.Sq + row] =
-        has_keys ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    const float lse_val = has_keys ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    const int64_t li = (static_cast<int64_t>(tl.b) * p.Hq + tl.h) * p.Sq + row;
+    if (partial)
+      p.lse_part[static_cast<int64_t>(tl.split) * p.B * p.Hq * p.Sq + li] = lse_val;
+    else
+      p.lse[li] = lse_val;
   }
   }  // work tiles
   if (p.stats != nullptr && lane == 0 && n_steps > 0) {

@@ -24,4 +24,14 @@ FA4_DECLARE_LAUNCH(launch_fwd_d64_traced)
 FA4_DECLARE_LAUNCH(launch_fwd_d128_traced)
 #undef FA4_DECLARE_LAUNCH
 
+// Largest number of key-range splits fa4_fwd_splitkv accepts.
+constexpr int kMaxSplits = 128;
+
+// Combine n_splits partial results (o_part [n][B][Sq][Hq][d] fp32 softmax-
+// normalised outputs, lse_part [n][B][Hq][Sq] natural-log LSE, -inf for an
+// empty split) into o (BF16) and lse.
+cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, __nv_bfloat16* o,
+                                float* lse, int n_splits, int B, int Sq, int Hq, int d,
+                                cudaStream_t stream);
+
 }  // namespace fa4

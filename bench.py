@@ -256,6 +256,11 @@ def run_ours(args, w: workloads.Workload) -> None:
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     kw = dict(tau=args.tau, exp2_emulation=args.exp2_emulation)
+    if args.num_splits:
+        kw.update(num_splits=args.num_splits,
+                  workspace=torch.empty(fa4.splitkv_workspace_bytes(w_rank.B, w.Hq, w.Sq, w.d,
+                                                                    args.num_splits),
+                                        dtype=torch.uint8, device=dev))
 
     def launch():
         fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
@@ -345,7 +350,8 @@ def run_ours(args, w: workloads.Workload) -> None:
             "data": "synthetic",
             "config": dict(w.describe(), global_batch=w.B * world, parallelism=f"replica-shards{world}",
                            l2="flushed before every timed launch (256 MiB write)",
-                           tau=args.tau, exp2_emulation=args.exp2_emulation),
+                           tau=args.tau, exp2_emulation=args.exp2_emulation,
+                           num_splits=args.num_splits),
             "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
@@ -357,7 +363,7 @@ def run_ours(args, w: workloads.Workload) -> None:
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.num_splits else 1),
         }
         print(json.dumps(line), flush=True)
     if pg:
@@ -374,6 +380,8 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--workload", default=workloads.LONG_CAUSAL.name,
                     choices=[x.name for x in workloads.ALL_NAMED])
     ap.add_argument("--tau", type=float, default=8.0)
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="key-range split forward with this many splits (0: plain forward)")
     ap.add_argument("--exp2-emulation", type=int, choices=[0, 4, 8], default=0,
                     help="one softmax entry pair in N through the software 2^x (0: none)")
     ap.add_argument("--e2e-steps", type=int, default=50)

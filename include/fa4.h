@@ -134,6 +134,45 @@ fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, floa
                       int causal, const fa4_fwd_options *opt, fa4_stream_t stream);
 
 /*
+ * fa4_fwd_splitkv -- the same forward, with the keys cut into num_splits
+ * contiguous ranges of whole 128-key blocks that separate CTAs process in
+ * parallel, then combined. Meant for shapes with few query tiles and many
+ * keys (short Sq, long Sk), where one CTA per query tile would leave SMs
+ * idle. The combine is exact: each range yields its softmax-normalised
+ * output O_s and logsumexp L_s, and
+ *     LSE = log sum_s exp(L_s),   O = sum_s exp(L_s - LSE) O_s
+ * is the softmax over the union of the ranges ("FlashAttention-4:
+ * Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware
+ * Scaling", Method: the output is recovered exactly at the final
+ * normalisation; here that normalisation is applied once more across key
+ * ranges -- the exchange step a key-parallel forward needs).
+ *
+ * Arguments as fa4_fwd, plus:
+ *   num_splits       1 .. 128 requested ranges (ranges that would start past
+ *                    the last key block are dropped; each range holds
+ *                    ceil(ceil(Sk / 128) / num_splits) blocks);
+ *   workspace        DEVICE scratch owned by the caller, 16-byte aligned,
+ *                    not overlapping any other argument, at least
+ *                    fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d,
+ *                    num_splits) bytes. Layout: fp32 partial outputs
+ *                    [num_splits][B][Sq][Hq][d], then fp32 partial LSE
+ *                    [num_splits][B][Hq][Sq]. Its contents on return are
+ *                    unspecified; it may be reused once the stream has
+ *                    passed this call.
+ *   opt              as fa4_fwd_ex (may be NULL).
+ * Enqueues two kernels (the split forward and the combine) on `stream`.
+ * Returns FA4_ERR_INVALID_ARG for a bad num_splits or a missing, small or
+ * overlapping workspace, FA4_ERR_MISALIGNED for a misaligned one, and
+ * otherwise as fa4_fwd_ex.
+ */
+uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_splits);
+fa4_status fa4_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                           int causal, int num_splits, void *workspace,
+                           uint64_t workspace_bytes, const fa4_fwd_options *opt,
+                           fa4_stream_t stream);
+
+/*
  * fa4_device_status -- synchronise the current device and return the
  * kernel-side status word: FA4_OK, or FA4_ERR_TIMEOUT if any kernel of
  * this library gave up on a pipeline wait since the last clear. `detail`

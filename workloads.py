@@ -83,9 +83,15 @@ def d64_sweep() -> List[Workload]:
 
 ALL_NAMED = [TINY, MID, LONG_CAUSAL, GQA_STRESS] + d64_sweep()
 
+# Few query tiles, many keys: 4 query-tile pairs per head x 16 heads = 64
+# work tiles on 152 SMs -- the shape the key-range split forward is for.
+SPLIT_LONG_KEYS = Workload("splitkv_fwd_b1_h16_sq1024_sk65536_d128", 1, 16, 16, 1024, 65536, 128,
+                           False)
+EXTRA = [SPLIT_LONG_KEYS]
+
 
 def by_name(name: str) -> Workload:
-    for w in ALL_NAMED:
+    for w in ALL_NAMED + EXTRA:
         if w.name == name:
             return w
     raise KeyError(name)
