@@ -81,6 +81,11 @@ def load_library():
     lib.fa4_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                     i32, vp, ctypes.c_uint64, ctypes.POINTER(_Options), vp]
     lib.fa4_fwd_splitkv.restype = i32
+    lib.fa4_fwd_splitkv_static_max_bytes.argtypes = []
+    lib.fa4_fwd_splitkv_static_max_bytes.restype = ctypes.c_uint64
+    lib.fa4_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                                           i32, i32, ctypes.POINTER(_Options), vp]
+    lib.fa4_fwd_splitkv_static.restype = i32
     lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa4_fwd_default_options.restype = None
     lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
@@ -184,6 +189,36 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                           lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
                           ctypes.byref(opt), _stream_handle(stream))
     _check(code, "fa4_fwd_ex")
+
+
+def fwd_splitkv_static_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                            lse: torch.Tensor, causal: bool, scale: Optional[float],
+                            num_splits: int, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """``fa4_fwd_splitkv_static``: the key-range split forward with the
+    library's own fixed device scratch (no workspace argument). Same tensor
+    rules as ``fwd_into``; default options."""
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Sq) or v.shape != k.shape:
+        raise ValueError("o must match q, v must match k and lse must be [B,Hq,Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = lib.fa4_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), B, Hq, Hkv, Sq, Sk, d, float(scale),
+                                      int(bool(causal)), int(num_splits), None,
+                                      _stream_handle(stream))
+    _check(code, "fa4_fwd_splitkv_static")
+
+
+def splitkv_static_max_bytes() -> int:
+    """Size of the library-held scratch of ``fwd_splitkv_static_into``."""
+    return int(load_library().fa4_fwd_splitkv_static_max_bytes())
 
 
 def splitkv_workspace_bytes(B: int, Hq: int, Sq: int, d: int, num_splits: int) -> int:

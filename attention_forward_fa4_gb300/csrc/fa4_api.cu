@@ -22,6 +22,11 @@ namespace {
 // Kernel-side status: [0] code, [1] role, [2] barrier id, [3] block.
 __device__ unsigned int g_status[4];
 
+// Library-owned scratch of fa4_fwd_splitkv_static: one fixed device array
+// per device, never allocated or freed at run time.
+constexpr uint64_t kStaticScratchBytes = 32ull << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
+
 constexpr int kMaxDevices = 64;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -44,6 +49,19 @@ EncodeTiledFn encode_fn() {
 }
 
 // Device address of g_status for the current device (looked up once each).
+// Device address of g_splitkv_scratch for the current device (looked up
+// once each, on the first fa4_fwd_splitkv_static call there).
+void* static_scratch_ptr(int dev) {
+  static std::atomic<void*> cache[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_splitkv_scratch) != cudaSuccess) return nullptr;
+  cache[dev].store(addr, std::memory_order_release);
+  return addr;
+}
+
 unsigned int* status_ptr(int dev) {
   static std::atomic<unsigned int*> cache[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -325,6 +343,26 @@ uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_s
   if (B < 0 || Hq < 0 || Sq < 0 || d < 0 || num_splits < 0) return 0;
   const uint64_t rows = static_cast<uint64_t>(num_splits) * B * Sq * Hq;
   return rows * static_cast<uint64_t>(d) * 4 + rows * 4;
+}
+
+uint64_t fa4_fwd_splitkv_static_max_bytes(void) { return fa4::kStaticScratchBytes; }
+
+fa4_status fa4_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                                  int causal, int num_splits, const fa4_fwd_options* opt,
+                                  fa4_stream_t stream) {
+  using namespace fa4;
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
+  if (fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits) > kStaticScratchBytes)
+    return FA4_ERR_INVALID_ARG;
+  fa4_status st = check_device();
+  if (st != FA4_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
+  void* scratch = static_scratch_ptr(dev);
+  if (!scratch) return FA4_ERR_CUDA;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, num_splits, scratch,
+                  static_cast<size_t>(kStaticScratchBytes), stream);
 }
 
 fa4_status fa4_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,

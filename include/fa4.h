@@ -173,6 +173,31 @@ fa4_status fa4_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
                            fa4_stream_t stream);
 
 /*
+ * fa4_fwd_splitkv_static -- fa4_fwd_splitkv without a caller workspace: the
+ * partial results go to a scratch array the library holds in device memory
+ * (a fixed-size file-scope __device__ array, one per device; nothing is
+ * allocated or freed at run time). The pages have no counterpart to this
+ * entry point; it exists for callers that cannot hand over a workspace.
+ *
+ * Arguments as fa4_fwd_splitkv without workspace / workspace_bytes. The
+ * scratch holds fa4_fwd_splitkv_static_max_bytes() bytes (32 MiB); a call
+ * whose fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits) exceeds it
+ * returns FA4_ERR_INVALID_ARG with nothing launched.
+ *
+ * The first call on each device looks up the scratch's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. All calls on a device share the one scratch array, so
+ * calls whose kernels can overlap in time -- on different streams, or from
+ * different host threads without ordering between their streams -- race on
+ * it and give undefined results. Calls on one stream are ordered and safe.
+ */
+uint64_t fa4_fwd_splitkv_static_max_bytes(void);
+fa4_status fa4_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o,
+                                  float *lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                                  float scale, int causal, int num_splits,
+                                  const fa4_fwd_options *opt, fa4_stream_t stream);
+
+/*
  * fa4_device_status -- synchronise the current device and return the
  * kernel-side status word: FA4_OK, or FA4_ERR_TIMEOUT if any kernel of
  * this library gave up on a pipeline wait since the last clear. `detail`
