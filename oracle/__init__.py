@@ -11,4 +11,6 @@ Contents:
                  conditional (lazy) rescale, in the pages' order.
   exp2_emu    -- model of the software 2^x (Cody-Waite range reduction +
                  Horner polynomial) with its own minimax fit.
+  splitkv     -- fp64 key-range forward and the LSE-weighted combine.
+  attn_bwd    -- fp64 gradient of attention (dQ, dK, dV) by the definition.
 """
