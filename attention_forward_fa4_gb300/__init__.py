@@ -86,6 +86,11 @@ def load_library():
     lib.fa4_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
                                            i32, i32, ctypes.POINTER(_Options), vp]
     lib.fa4_fwd_splitkv_static.restype = i32
+    lib.fa4_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.fa4_bwd_workspace_bytes.restype = ctypes.c_uint64
+    lib.fa4_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                            vp, ctypes.c_uint64, vp]
+    lib.fa4_bwd.restype = i32
     lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa4_fwd_default_options.restype = None
     lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
@@ -219,6 +224,56 @@ def fwd_splitkv_static_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o
 def splitkv_static_max_bytes() -> int:
     """Size of the library-held scratch of ``fwd_splitkv_static_into``."""
     return int(load_library().fa4_fwd_splitkv_static_max_bytes())
+
+
+def bwd_workspace_bytes(B: int, Hq: int, Sq: int, d: int) -> int:
+    """Device scratch bytes the backward needs."""
+    return int(load_library().fa4_bwd_workspace_bytes(B, Hq, Sq, d))
+
+
+def bwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             dout: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+             dv: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
+             workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """``fa4_bwd``: write dq, dk, dv (preallocated, BF16) for the upstream
+    gradient ``dout``; ``o`` and ``lse`` are the forward's outputs.
+    ``workspace`` (CUDA uint8) is allocated here when omitted."""
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("dout", dout, torch.bfloat16), ("lse", lse, torch.float32),
+                        ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16),
+                        ("dv", dv, torch.bfloat16)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if (o.shape != q.shape or dout.shape != q.shape or dq.shape != q.shape or v.shape != k.shape
+            or dk.shape != k.shape or dv.shape != k.shape or tuple(lse.shape) != (B, Hq, Sq)):
+        raise ValueError("shapes: q, o, dout, dq [B,Sq,Hq,d]; k, v, dk, dv [B,Sk,Hkv,d]; "
+                         "lse [B,Hq,Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bwd_workspace_bytes(B, Hq, Sq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    code = lib.fa4_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq,
+                       Sk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                       workspace.numel(), _stream_handle(stream))
+    _check(code, "fa4_bwd")
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+        lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, **kw
+        ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Attention backward; returns (dq, dk, dv)."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bwd_into(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, **kw)
+    return dq, dk, dv
 
 
 def splitkv_workspace_bytes(B: int, Hq: int, Sq: int, d: int, num_splits: int) -> int:

@@ -345,6 +345,86 @@ uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_s
   return rows * static_cast<uint64_t>(d) * 4 + rows * 4;
 }
 
+uint64_t fa4_bwd_workspace_bytes(int B, int Hq, int Sq, int d) {
+  if (B < 0 || Hq < 0 || Sq < 0 || d < 0) return 0;
+  const uint64_t sq_pad = (static_cast<uint64_t>(Sq) + 127) / 128 * 128;
+  return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4;
+}
+
+fa4_status fa4_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+                   int Sk, int d, float scale, int causal, void* workspace,
+                   uint64_t workspace_bytes, fa4_stream_t stream) {
+  using namespace fa4;
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return FA4_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA4_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA4_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FA4_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
+  if (B == 0 || (Sq == 0 && Sk == 0)) return FA4_OK;
+  const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
+  const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
+  const uint64_t lse_bytes = static_cast<uint64_t>(B) * Hq * Sq * 4;
+  const bool has_q = Sq > 0, has_k = Sk > 0;
+  if ((has_q && (!q || !o || !dout || !lse || !dq)) || (has_k && (!k || !v || !dk || !dv)))
+    return FA4_ERR_INVALID_ARG;
+  auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if ((has_q && (mis16(q) || mis16(o) || mis16(dout) || mis16(dq) ||
+                 (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)) ||
+      (has_k && (mis16(k) || mis16(v) || mis16(dk) || mis16(dv))))
+    return FA4_ERR_MISALIGNED;
+  const uint64_t need = fa4_bwd_workspace_bytes(B, Hq, Sq, d);
+  if (has_q && has_k) {
+    if (!workspace || workspace_bytes < need) return FA4_ERR_INVALID_ARG;
+    if (mis16(workspace)) return FA4_ERR_MISALIGNED;
+  }
+  // Outputs overlap nothing: not the inputs, not each other, not the workspace.
+  const void* ins[] = {q, k, v, o, dout, lse};
+  const uint64_t in_n[] = {q_bytes, kv_bytes, kv_bytes, q_bytes, q_bytes, lse_bytes};
+  const void* outs[] = {dq, dk, dv, (has_q && has_k) ? workspace : nullptr};
+  const uint64_t out_n[] = {q_bytes, kv_bytes, kv_bytes, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_n[a], ins[b], in_n[b])) return FA4_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return FA4_ERR_INVALID_ARG;
+  }
+  const int64_t n_kblk = (static_cast<int64_t>(Sk) + 127) / 128;
+  if (n_kblk * B * Hkv > 0x7fffffffLL) return FA4_ERR_UNSUPPORTED;
+  if (static_cast<uint64_t>(Sq) * Hq * d * 2 >= (1ull << 40) ||
+      static_cast<uint64_t>(Sk) * Hkv * d * 2 >= (1ull << 40))
+    return FA4_ERR_UNSUPPORTED;
+
+  fa4_status st = check_device();
+  if (st != FA4_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
+  unsigned int* status = status_ptr(dev);
+  if (!status) return FA4_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!has_q || !has_k) {
+    // no queries: dK = dV = 0; no keys: the output is constant 0, dQ = 0
+    if (has_k && (cudaMemsetAsync(dk, 0, kv_bytes, s) != cudaSuccess ||
+                  cudaMemsetAsync(dv, 0, kv_bytes, s) != cudaSuccess))
+      return FA4_ERR_CUDA;
+    if (has_q && cudaMemsetAsync(dq, 0, q_bytes, s) != cudaSuccess) return FA4_ERR_CUDA;
+    return FA4_OK;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
+      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map(&tdo, dout, B, Sq, Hq, d))
+    return FA4_ERR_CUDA;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
+  float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);
+  cudaError_t err = launch_bwd(tq, tk, tv, tdo, static_cast<const __nv_bfloat16*>(o),
+                               static_cast<const __nv_bfloat16*>(dout), lse,
+                               static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+                               static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta, B, Hq, Hkv, Sq,
+                               Sk, d, scale, causal != 0, status, s);
+  return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
+}
+
 uint64_t fa4_fwd_splitkv_static_max_bytes(void) { return fa4::kStaticScratchBytes; }
 
 fa4_status fa4_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -1,0 +1,413 @@
+// fa4_bwd_kernel.cuh -- attention backward on sm_103a: dQ, dK, dV from Q,
+// K, V, dO and the forward's logsumexp, with tcgen05 MMAs into tensor
+// memory ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+// Asymmetric Hardware Scaling", §3.2: five MMAs per tile pair).
+//
+// One CTA owns a 128-key block of one (batch, kv head) and walks every
+// query block of every query head that reads it. Per step (128 queries x
+// 128 keys), with rows of the transposed products on TMEM lanes = keys:
+//
+//   S^T  = K Q^T            SS MMA          TMEM cols [0, 128)
+//   dP^T = V dO^T           SS MMA          TMEM cols [128, 256)
+//   P^T  = 2^(c S^T - LSE2) (softmax WG, one key row per thread; masked 0)
+//   dS^T = P^T o (dP^T - Delta)
+//   dV  += P^T dO           TS MMA, A = P^T from TMEM (BF16 over S^T)
+//   dK  += dS^T Q           TS MMA, A = dS^T from TMEM (BF16 over dP^T)
+//   dQ   = dS K             SS MMA, A = dS from shared memory (MN-major,
+//                           written by the softmax threads), into cols
+//                           [0, D) over S^T; read out and added atomically
+//                           (fp32) to the global dQ accumulator.
+//
+// dK and dV accumulate in TMEM (cols [256, 256 + 2D)) over all steps and
+// are written once at the end; the GQA group's query heads all pass through
+// the CTA, so kv-head gradients need no atomics. Delta_i = sum_e dO O and
+// LSE2 = LSE log2(e) (+inf for rows that must contribute nothing) come from
+// a preprocessing kernel, padded to whole 128-row blocks.
+//
+// Warps: 0-3 softmax-side work and the dK/dV epilogue, 4-7 dQ read-out and
+// atomics, 8 TMA loads, 9 MMA issue (both warp-wide with an elected lane),
+// 10-11 idle. Every wait is bounded (Waiter), as in the forward kernel.
+#pragma once
+
+#include "fa4_fwd_kernel.cuh"
+
+namespace fa4 {
+
+constexpr int kBwdThreads = 384;
+constexpr int kBwdWarpLoad = 8;
+constexpr int kBwdWarpMma = 9;
+
+struct BwdParams {
+  __nv_bfloat16* dk;        // [B, Sk, Hkv, D]
+  __nv_bfloat16* dv;        // [B, Sk, Hkv, D]
+  float* dq_acc;            // [B, Sq, Hq, D] fp32, zeroed; receives scale * dS K
+  const float* lse2;        // [B * Hq][Sq_pad]
+  const float* delta;       // [B * Hq][Sq_pad]
+  int B, Hq, Hkv, Sq, Sk, group, Sq_pad, n_kblk;
+  float scale, scale_log2;
+  unsigned int* status;
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kPanelBytes = 128 * 128;
+  static constexpr int kPanels = D / 64;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;
+  static constexpr int kDO = kQ + kTileBytes;
+  static constexpr int kDS = kDO + kTileBytes;          // 128 x 128 BF16, two MN-major panels
+  static constexpr int kLse = kDS + 2 * kPanelBytes;     // float [128]
+  static constexpr int kDelta = kLse + 512;              // float [128]
+  static constexpr int kBars = kDelta + 512;
+  static constexpr int bKv = 0, bQdo = 1, bQdoEmpty = 2, bSdp = 3, bPReady = 4, bDqFull = 5,
+                       bDqFree = 6, bAcc = 7, kNumBars = 8;
+  static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+// The CTA's key block and the query blocks it visits.
+struct BwdWork {
+  int b, g, k0;
+  int qb0, n_qb;      // query blocks [qb0, n_qb) of every head in the group
+  int steps;          // group * (n_qb - qb0)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
+  BwdWork w;
+  const int id = static_cast<int>(blockIdx.x);
+  const int kb = id % p.n_kblk;
+  const int bg = id / p.n_kblk;
+  w.b = bg / p.Hkv;
+  w.g = bg - w.b * p.Hkv;
+  w.k0 = kb * 128;
+  w.n_qb = (p.Sq + 127) / 128;
+  w.qb0 = 0;
+  if (CAUSAL) {
+    // the first query that sees key k0: i >= k0 - (Sk - Sq)
+    const long long i_min = static_cast<long long>(w.k0) - (p.Sk - p.Sq);
+    w.qb0 = i_min <= 0 ? 0 : static_cast<int>(i_min / 128 < w.n_qb ? i_min / 128 : w.n_qb);
+  }
+  w.steps = p.group * (w.n_qb - w.qb0);
+  return w;
+}
+
+// ------------------------------------------------------------ load warp
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void bwd_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_v, const CUtensorMap* tm_do,
+                                              uint32_t sbase, const BwdParams& p, const Waiter& w) {
+  using L = BwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const BwdWork wk = bwd_work<CAUSAL>(p);
+  if (wk.steps == 0) return;
+  mbar_arrive_expect_tx_warp(bar(L::bKv), 2u * L::kTileBytes);
+#pragma unroll
+  for (int pn = 0; pn < L::kPanels; ++pn) {
+    tma_load_4d_warp(sbase + L::kK + pn * L::kPanelBytes, tm_k, bar(L::bKv), pn * 64, wk.g, wk.k0, wk.b);
+    tma_load_4d_warp(sbase + L::kV + pn * L::kPanelBytes, tm_v, bar(L::bKv), pn * 64, wk.g, wk.k0, wk.b);
+  }
+  const int per_head = wk.n_qb - wk.qb0;
+  bool ok = true;
+  int s = 0;
+  for (; s < wk.steps; ++s) {
+    const int h = wk.g * p.group + s / per_head;
+    const int qb = wk.qb0 + s % per_head;
+    if (s > 0 && !(ok = w.wait_warp(bar(L::bQdoEmpty), static_cast<uint32_t>(s - 1) & 1u, L::bQdoEmpty)))
+      break;
+    mbar_arrive_expect_tx_warp(bar(L::bQdo), 2u * L::kTileBytes + 1024u);
+#pragma unroll
+    for (int pn = 0; pn < L::kPanels; ++pn) {
+      tma_load_4d_warp(sbase + L::kQ + pn * L::kPanelBytes, tm_q, bar(L::bQdo), pn * 64, h, qb * 128, wk.b);
+      tma_load_4d_warp(sbase + L::kDO + pn * L::kPanelBytes, tm_do, bar(L::bQdo), pn * 64, h, qb * 128,
+                       wk.b);
+    }
+    const int64_t row0 = (static_cast<int64_t>(wk.b) * p.Hq + h) * p.Sq_pad + qb * 128;
+    bulk_load_warp(sbase + L::kLse, p.lse2 + row0, 512u, bar(L::bQdo));
+    bulk_load_warp(sbase + L::kDelta, p.delta + row0, 512u, bar(L::bQdo));
+  }
+  if (__any_sync(0xffffffffu, !ok || *w.abort)) {
+    // Let the copies this warp started land before the CTA exits.
+    w.drain_warp(bar(L::bKv), 0u, L::bKv);
+    if (s > 0) w.drain_warp(bar(L::bQdo), static_cast<uint32_t>(s - 1) & 1u, L::bQdo);
+  }
+}
+
+// ------------------------------------------------------------ MMA warp
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, const BwdParams& p,
+                                             const Waiter& w) {
+  using L = BwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const BwdWork wk = bwd_work<CAUSAL>(p);
+  if (wk.steps == 0) return;
+  constexpr uint32_t kIdescKmaj = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+  constexpr uint32_t kIdescTs = idesc_bf16_f32(128, D, false, true);        // dV, dK
+  constexpr uint32_t kIdescDq = idesc_bf16_f32(128, D, true, true);         // dQ: A, B MN-major
+  constexpr uint32_t kHi = desc_hi_sw128(1024);
+  // K-major views (LBO unused) and MN-major views (LBO = 64-column panel stride).
+  const uint32_t k_lo = desc_lo_sw128(sbase + L::kK, 16), v_lo = desc_lo_sw128(sbase + L::kV, 16);
+  const uint32_t q_lo = desc_lo_sw128(sbase + L::kQ, 16), do_lo = desc_lo_sw128(sbase + L::kDO, 16);
+  const uint32_t q_mn = desc_lo_sw128(sbase + L::kQ, L::kPanelBytes);
+  const uint32_t do_mn = desc_lo_sw128(sbase + L::kDO, L::kPanelBytes);
+  const uint32_t k_mn = desc_lo_sw128(sbase + L::kK, L::kPanelBytes);
+  const uint32_t ds_mn = desc_lo_sw128(sbase + L::kDS, L::kPanelBytes);
+  bool ok = w.wait_warp(bar(L::bKv), 0u, L::bKv);
+  tc_fence_after_sync();
+  for (int s = 0; ok && s < wk.steps; ++s) {
+    if (!(ok = w.wait_warp(bar(L::bQdo), static_cast<uint32_t>(s) & 1u, L::bQdo))) break;
+    if (s > 0 && !(ok = w.wait_warp(bar(L::bDqFree), static_cast<uint32_t>(s - 1) & 1u, L::bDqFree)))
+      break;
+    tc_fence_after_sync();
+    // S^T = K Q^T and dP^T = V dO^T (keys on the M side, queries on N)
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+      mma_ss_lohi_warp(tmem + L::kColS, k_lo + off, kHi, q_lo + off, kHi, kIdescKmaj, kk > 0 ? 1u : 0u);
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+      mma_ss_lohi_warp(tmem + L::kColDP, v_lo + off, kHi, do_lo + off, kHi, kIdescKmaj, kk > 0 ? 1u : 0u);
+    }
+    mma_commit_warp(bar(L::bSdp));
+    if (!(ok = w.wait_warp(bar(L::bPReady), static_cast<uint32_t>(s) & 1u, L::bPReady))) break;
+    tc_fence_after_sync();
+    // dV += P^T dO and dK += dS^T Q: 16 queries (8 TMEM columns of packed
+    // BF16, 2 KB of the MN-major operand) per MMA
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts_lohi_warp(tmem + L::kColDV, tmem + L::kColS + kk * 8, do_mn + kk * (2048 >> 4), kHi, kIdescTs,
+                       (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts_lohi_warp(tmem + L::kColDK, tmem + L::kColDP + kk * 8, q_mn + kk * (2048 >> 4), kHi, kIdescTs,
+                       (s > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_warp(bar(L::bQdoEmpty));
+    // dQ = dS K over the S^T columns: issued after the dV MMA that reads
+    // P^T there (one issuing thread's MMAs execute in order)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lohi_warp(tmem + L::kColS, ds_mn + kk * (2048 >> 4), kHi, k_mn + kk * (2048 >> 4), kHi, kIdescDq,
+                       kk > 0 ? 1u : 0u);
+    mma_commit_warp(bar(L::bDqFull));
+  }
+  // Every MMA issued above has completed once this commit arrives (the
+  // epilogue waits for it; on abort it is the drain).
+  mma_commit_warp(bar(L::bAcc));
+  w.drain_warp(bar(L::bAcc), 0u, L::bAcc);
+}
+
+// ------------------------------------------------------------ softmax-side WG
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void bwd_softmax_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                                                 const BwdParams& p, const Waiter& w) {
+  using L = BwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = warp * 32 + lane;                       // key row of the block = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const int kabs = wk.k0 + r;
+  const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
+  const float* delta_s = reinterpret_cast<const float*>(smem + L::kDelta);
+  const float c2 = p.scale_log2;
+  const int shift = p.Sk - p.Sq;
+  const int per_head = wk.n_qb - wk.qb0;
+  bool ok = true;
+  for (int s = 0; s < wk.steps; ++s) {
+    const int q0 = (wk.qb0 + s % per_head) * 128;
+    if (!(ok = w.wait(bar(L::bQdo), static_cast<uint32_t>(s) & 1u, L::bQdo))) break;
+    if (!(ok = w.wait(bar(L::bSdp), static_cast<uint32_t>(s) & 1u, L::bSdp))) break;
+    tc_fence_after_sync();
+    // whole block visible to this key row (tile-uniform tests keep the mask off the common path)
+    const bool row_live = kabs < p.Sk;
+    const bool all_visible = !CAUSAL || (wk.k0 + 127 <= q0 + shift);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t sv[32], dv[32];
+      tmem_ld_x32(lane_base + L::kColS + 32 * c, sv);
+      tmem_ld_x32(lane_base + L::kColDP + 32 * c, dv);
+      tmem_wait_ld_x32(sv);
+      tmem_wait_ld_x32(dv);
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const int qi = 32 * c + e;
+        float p0 = ex2_mufu(__uint_as_float(sv[e]) * c2 - lse_s[qi]);
+        float p1 = ex2_mufu(__uint_as_float(sv[e + 1]) * c2 - lse_s[qi + 1]);
+        if (!row_live || (!all_visible && kabs > q0 + qi + shift)) p0 = 0.0f;
+        if (!row_live || (!all_visible && kabs > q0 + qi + 1 + shift)) p1 = 0.0f;
+        const float d0 = p0 * (__uint_as_float(dv[e]) - delta_s[qi]);
+        const float d1 = p1 * (__uint_as_float(dv[e + 1]) - delta_s[qi + 1]);
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+        dk[e >> 1] = pack_bf16x2(d0, d1);
+      }
+      // P^T over S^T, dS^T over dP^T (columns already read)
+      tmem_st_x16(lane_base + L::kColS + 16 * c, pk);
+      tmem_st_x16(lane_base + L::kColDP + 16 * c, dk);
+      // dS for the dQ MMA: MN-major A tile, panel = 64 queries, row = key,
+      // 128-byte swizzle (16-byte chunk index XOR row within its 8-row group)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int chunk = 4 * (c & 1) + u;
+        const uint32_t addr = sbase + L::kDS + (c >> 1) * L::kPanelBytes + r * 128 +
+                              (static_cast<uint32_t>(chunk ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk[4 * u]),
+                     "r"(dk[4 * u + 1]), "r"(dk[4 * u + 2]), "r"(dk[4 * u + 3])
+                     : "memory");
+      }
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    mbar_arrive(bar(L::bPReady));
+  }
+  // ---- epilogue: dV, scale * dK -> BF16 -> global
+  const bool row_ok = kabs < p.Sk;
+  const int64_t orow = (static_cast<int64_t>(wk.b) * p.Sk + kabs) * p.Hkv + wk.g;
+  __nv_bfloat16* dv_row = p.dv + orow * D;
+  __nv_bfloat16* dk_row = p.dk + orow * D;
+  if (ok && wk.steps > 0) {
+    if (!w.wait(bar(L::bAcc), 0u, L::bAcc)) return;
+    tc_fence_after_sync();
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t x[32], y[32];
+      tmem_ld_x32(lane_base + L::kColDV + 32 * c, x);
+      tmem_ld_x32(lane_base + L::kColDK + 32 * c, y);
+      tmem_wait_ld_x32(x);
+      tmem_wait_ld_x32(y);
+      if (row_ok) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 a, b;
+          a.x = pack_bf16x2(__uint_as_float(x[8 * i + 0]), __uint_as_float(x[8 * i + 1]));
+          a.y = pack_bf16x2(__uint_as_float(x[8 * i + 2]), __uint_as_float(x[8 * i + 3]));
+          a.z = pack_bf16x2(__uint_as_float(x[8 * i + 4]), __uint_as_float(x[8 * i + 5]));
+          a.w = pack_bf16x2(__uint_as_float(x[8 * i + 6]), __uint_as_float(x[8 * i + 7]));
+          b.x = pack_bf16x2(__uint_as_float(y[8 * i + 0]) * p.scale, __uint_as_float(y[8 * i + 1]) * p.scale);
+          b.y = pack_bf16x2(__uint_as_float(y[8 * i + 2]) * p.scale, __uint_as_float(y[8 * i + 3]) * p.scale);
+          b.z = pack_bf16x2(__uint_as_float(y[8 * i + 4]) * p.scale, __uint_as_float(y[8 * i + 5]) * p.scale);
+          b.w = pack_bf16x2(__uint_as_float(y[8 * i + 6]) * p.scale, __uint_as_float(y[8 * i + 7]) * p.scale);
+          reinterpret_cast<uint4*>(dv_row + c * 32)[i] = a;
+          reinterpret_cast<uint4*>(dk_row + c * 32)[i] = b;
+        }
+      }
+    }
+  } else if (ok && row_ok) {
+    // no query reads this key block: zero gradients
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      reinterpret_cast<uint4*>(dv_row)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(dk_row)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// ------------------------------------------------------------ dQ read-out WG
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void bwd_dq_role(uint32_t sbase, uint32_t tmem, const BwdParams& p,
+                                            const Waiter& w) {
+  using L = BwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int r = wq * 32 + lane;                         // query row of the block = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const int per_head = wk.n_qb - wk.qb0;
+  for (int s = 0; s < wk.steps; ++s) {
+    const int h = wk.g * p.group + s / per_head;
+    const int row = (wk.qb0 + s % per_head) * 128 + r;
+    if (!w.wait(bar(L::bDqFull), static_cast<uint32_t>(s) & 1u, L::bDqFull)) return;
+    tc_fence_after_sync();
+    uint32_t x[D];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c)
+      tmem_ld_x32(lane_base + L::kColS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+    // dQ is in registers: the next step's S^T may overwrite its columns
+    tc_fence_before_sync();
+    mbar_arrive(bar(L::bDqFree));
+    if (row < p.Sq) {
+      float* dst = p.dq_acc + ((static_cast<int64_t>(wk.b) * p.Sq + row) * p.Hq + h) * D;
+#pragma unroll
+      for (int e = 0; e < D; e += 4)
+        red_add_v4(dst + e, __uint_as_float(x[e]) * p.scale, __uint_as_float(x[e + 1]) * p.scale,
+                   __uint_as_float(x[e + 2]) * p.scale, __uint_as_float(x[e + 3]) * p.scale);
+    }
+  }
+}
+
+// ------------------------------------------------------------ kernel
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa4_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    mbar_init(bar(L::bKv), 1);
+    mbar_init(bar(L::bQdo), 1);
+    mbar_init(bar(L::bQdoEmpty), 1);
+    mbar_init(bar(L::bSdp), 1);
+    mbar_init(bar(L::bPReady), 128);
+    mbar_init(bar(L::bDqFull), 1);
+    mbar_init(bar(L::bDqFree), 128);
+    mbar_init(bar(L::bAcc), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kBwdWarpLoad && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    const Waiter w{abort_flag, p.status, kRoleSoftmax};
+    bwd_softmax_role<D, CAUSAL>(sbase, smem, tmem, p, w);
+  } else if (warp < 8) {
+    const Waiter w{abort_flag, p.status, kRoleCorrection};
+    bwd_dq_role<D, CAUSAL>(sbase, tmem, p, w);
+  } else if (warp == kBwdWarpLoad) {
+    const Waiter w{abort_flag, p.status, kRoleLoad};
+    bwd_load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, &tm_do, sbase, p, w);
+  } else if (warp == kBwdWarpMma) {
+    const Waiter w{abort_flag, p.status, kRoleMma};
+    bwd_mma_role<D, CAUSAL>(sbase, tmem, p, w);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa4

@@ -24,6 +24,15 @@ FA4_DECLARE_LAUNCH(launch_fwd_d64_traced)
 FA4_DECLARE_LAUNCH(launch_fwd_d128_traced)
 #undef FA4_DECLARE_LAUNCH
 
+// Attention backward (fa4_bwd.cu): zero dq_acc, preprocess (lse2, delta),
+// main kernel (dK, dV, atomic dQ), dq_acc -> dq.
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                       const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
+                       float* dq_acc, float* lse2, float* delta, int B, int Hq, int Hkv, int Sq,
+                       int Sk, int d, float scale, bool causal, unsigned int* status,
+                       cudaStream_t s);
+
 // Largest number of key-range splits fa4_fwd_splitkv accepts.
 constexpr int kMaxSplits = 128;
 

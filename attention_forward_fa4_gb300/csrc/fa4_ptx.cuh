@@ -118,6 +118,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_
       : "memory");
 }
 
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completing that many bytes on `bar`; issued by
+// one elected lane of a converged warp.
+__device__ __forceinline__ void bulk_load_warp(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (tcgen05.mma operand reads) that a barrier hands them to.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four fp32 atomic adds to consecutive global addresses (16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // Whole-warp instructions (.sync.aligned).
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

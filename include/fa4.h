@@ -134,6 +134,37 @@ fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, floa
                       int causal, const fa4_fwd_options *opt, fa4_stream_t stream);
 
 /*
+ * fa4_bwd -- attention backward: the gradients of O = softmax(scale QK^T
+ * [+causal]) V with respect to q, k, v for an upstream gradient dout
+ * ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+ * Asymmetric Hardware Scaling", §3.2: five MMAs per tile pair -- S, dP,
+ * dV += P^T dO, dK += dS^T Q, dQ += dS K -- with
+ * dS = P o (dP - rowsum(dO o O))).
+ *
+ *   q, o, dout       [B, Sq, Hq, d]  BF16, device, 16-byte aligned (o and lse
+ *                    are the forward's outputs for these q, k, v)
+ *   k, v             [B, Sk, Hkv, d] BF16, device, 16-byte aligned
+ *   lse              [B, Hq, Sq]     fp32 natural-log LSE, 4-byte aligned
+ *   dq               [B, Sq, Hq, d]  BF16, written
+ *   dk, dv           [B, Sk, Hkv, d] BF16, written (a kv head's gradient sums
+ *                    over the query heads of its group)
+ *   workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
+ *                    least fa4_bwd_workspace_bytes(B, Hq, Sq, d) bytes: the
+ *                    fp32 dQ accumulator [B, Sq, Hq, d], then LSE log2(e)
+ *                    and rowsum(dO o O), each [B, Hq, Sq rounded up to 128].
+ *   other arguments and rules as fa4_fwd; dq, dk, dv and the workspace
+ *   must not overlap each other or any input.
+ * Enqueues a memset, a preprocessing kernel, the main kernel and a
+ * conversion kernel on `stream`. Sq == 0 gives dk = dv = 0; Sk == 0 gives
+ * dq = 0.
+ */
+uint64_t fa4_bwd_workspace_bytes(int B, int Hq, int Sq, int d);
+fa4_status fa4_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                   int Sq, int Sk, int d, float scale, int causal, void *workspace,
+                   uint64_t workspace_bytes, fa4_stream_t stream);
+
+/*
  * fa4_fwd_splitkv -- the same forward, with the keys cut into num_splits
  * contiguous ranges of whole 128-key blocks that separate CTAs process in
  * parallel, then combined. Meant for shapes with few query tiles and many
