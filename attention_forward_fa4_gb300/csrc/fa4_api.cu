@@ -109,6 +109,23 @@ bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [B, S, H, d] tensor (the backward's dQ accumulator) as a 4-D map with
+// a 32-column x 128-row box and 128-byte swizzle (32 fp32 = 128 bytes).
+bool make_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(H) * d * 4,
+                                 static_cast<cuuint64_t>(S) * H * d * 4};
+  const cuuint32_t box[4] = {32, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -410,14 +427,15 @@ fa4_status fa4_bwd(const void* q, const void* k, const void* v, const void* o, c
     if (has_q && cudaMemsetAsync(dq, 0, q_bytes, s) != cudaSuccess) return FA4_ERR_CUDA;
     return FA4_OK;
   }
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
-      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map(&tdo, dout, B, Sq, Hq, d))
-    return FA4_ERR_CUDA;
   float* dq_acc = static_cast<float*>(workspace);
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
+      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map(&tdo, dout, B, Sq, Hq, d) ||
+      !make_map_f32(&tdq, dq_acc, B, Sq, Hq, d))
+    return FA4_ERR_CUDA;
   float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
   float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);
-  cudaError_t err = launch_bwd(tq, tk, tv, tdo, static_cast<const __nv_bfloat16*>(o),
+  cudaError_t err = launch_bwd(tq, tk, tv, tdo, tdq, static_cast<const __nv_bfloat16*>(o),
                                static_cast<const __nv_bfloat16*>(dout), lse,
                                static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta, B, Hq, Hkv, Sq,
@@ -469,7 +487,7 @@ fa4_status fa4_device_status(int clear, unsigned int* detail) {
     const unsigned int z[4] = {0, 0, 0, 0};
     if (cudaMemcpyToSymbol(g_status, z, sizeof z) != cudaSuccess) return FA4_ERR_CUDA;
   }
-  return h[0] == 0 ? FA4_OK : FA4_ERR_TIMEOUT;
+  return h[0] == 0 ? FA4_OK : static_cast<fa4_status>(h[0]);
 }
 
 fa4_status fa4_exp2_eval(const float* x, float* y_emu, float* y_mufu, int64_t n,

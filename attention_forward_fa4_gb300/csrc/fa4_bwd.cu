@@ -63,19 +63,21 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
 
 template <int D, bool CAUSAL>
 cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const CUtensorMap& tdo, const BwdParams& p, unsigned grid, cudaStream_t s) {
+                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                        unsigned grid, cudaStream_t s) {
   constexpr int kSmem = BwdSmem<D>::kAlloc;
   auto kernel = fa4_bwd_kernel<D, CAUSAL>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
-  kernel<<<grid, kBwdThreads, kSmem, s>>>(tq, tk, tv, tdo, p);
+  kernel<<<grid, kBwdThreads, kSmem, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
+                       const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
                        float* dq_acc, float* lse2, float* delta, int B, int Hq, int Hkv, int Sq,
                        int Sk, int d, float scale, bool causal, unsigned int* status,
@@ -111,11 +113,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.status = status;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(p.n_kblk) * B * Hkv);
   if (d == 64)
-    err = causal ? launch_main<64, true>(tq, tk, tv, tdo, p, grid, s)
-                 : launch_main<64, false>(tq, tk, tv, tdo, p, grid, s);
+    err = causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                 : launch_main<64, false>(tq, tk, tv, tdo, tdq, p, grid, s);
   else
-    err = causal ? launch_main<128, true>(tq, tk, tv, tdo, p, grid, s)
-                 : launch_main<128, false>(tq, tk, tv, tdo, p, grid, s);
+    err = causal ? launch_main<128, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                 : launch_main<128, false>(tq, tk, tv, tdo, tdq, p, grid, s);
   if (err != cudaSuccess) return err;
 
   const int64_t n4 = dq_elems / 4;

@@ -9,14 +9,18 @@
 //
 //   S^T  = K Q^T            SS MMA          TMEM cols [0, 128)
 //   dP^T = V dO^T           SS MMA          TMEM cols [128, 256)
-//   P^T  = 2^(c S^T - LSE2) (softmax WG, one key row per thread; masked 0)
+//   P^T  = 2^(c S^T - LSE2) (compute warps, one key row per thread and
+//                           half the queries per warp; masked 0)
 //   dS^T = P^T o (dP^T - Delta)
-//   dV  += P^T dO           TS MMA, A = P^T from TMEM (BF16 over S^T)
-//   dK  += dS^T Q           TS MMA, A = dS^T from TMEM (BF16 over dP^T)
+//   dV  += P^T dO           TS MMA, A = P^T from TMEM (BF16 over S^T: the
+//                           32 queries of each 32-column chunk in its first
+//                           16 columns)
+//   dK  += dS^T Q           TS MMA, A = dS^T from TMEM (BF16 over dP^T, same)
 //   dQ   = dS K             SS MMA, A = dS from shared memory (MN-major,
-//                           written by the softmax threads), into cols
-//                           [0, D) over S^T; read out and added atomically
-//                           (fp32) to the global dQ accumulator.
+//                           written by the compute threads), into cols
+//                           [0, D) over S^T; read out, staged in shared
+//                           memory and added to the global fp32 dQ
+//                           accumulator with bulk tensor reduce-adds.
 //
 // dK and dV accumulate in TMEM (cols [256, 256 + 2D)) over all steps and
 // are written once at the end; the GQA group's query heads all pass through
@@ -24,9 +28,10 @@
 // LSE2 = LSE log2(e) (+inf for rows that must contribute nothing) come from
 // a preprocessing kernel, padded to whole 128-row blocks.
 //
-// Warps: 0-3 softmax-side work and the dK/dV epilogue, 4-7 dQ read-out and
-// atomics, 8 TMA loads, 9 MMA issue (both warp-wide with an elected lane),
-// 10-11 idle. Every wait is bounded (Waiter), as in the forward kernel.
+// Warps: 0-7 softmax-side work, dQ read-out and atomics, and the dK/dV
+// epilogue (two warps per TMEM lane quarter, each on half of the columns);
+// 8 TMA loads, 9 MMA issue (both warp-wide with an elected lane); 10-11
+// idle. Every wait is bounded (Waiter), as in the forward kernel.
 #pragma once
 
 #include "fa4_fwd_kernel.cuh"
@@ -48,26 +53,38 @@ struct BwdParams {
   unsigned int* status;
 };
 
+// Q, dO, LSE2 and Delta of a step sit in one of kStages stages (two at
+// d = 64, so the next step's copies land while the current step computes;
+// one at d = 128, where the space goes to the dQ staging tile). The dQ
+// staging tile holds a step's fp32 dQ in 32-column, 128-byte-swizzled
+// blocks for the bulk reduce-add into the global accumulator.
 template <int D>
 struct BwdSmem {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kPanelBytes = 128 * 128;
   static constexpr int kPanels = D / 64;
+  static constexpr int kStages = D == 128 ? 1 : 2;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;
-  static constexpr int kDO = kQ + kTileBytes;
-  static constexpr int kDS = kDO + kTileBytes;          // 128 x 128 BF16, two MN-major panels
-  static constexpr int kLse = kDS + 2 * kPanelBytes;     // float [128]
-  static constexpr int kDelta = kLse + 512;              // float [128]
-  static constexpr int kBars = kDelta + 512;
-  static constexpr int bKv = 0, bQdo = 1, bQdoEmpty = 2, bSdp = 3, bPReady = 4, bDqFull = 5,
-                       bDqFree = 6, bAcc = 7, kNumBars = 8;
+  static constexpr int kDS = kV + kTileBytes;           // 128 x 128 BF16, two MN-major panels
+  static constexpr int kDqStage = kDS + 2 * kPanelBytes;  // (D / 32) x [128 rows x 32 fp32]
+  static constexpr int kStage = kDqStage + 128 * D * 4;   // kStages x {Q, dO, LSE2, Delta}
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kQ = 0, kDO = kTileBytes, kLse = 2 * kTileBytes, kDelta = kLse + 512;
+  static constexpr int kBars = kStage + kStages * kStageBytes;
+  // barriers: kv, qdo[2], qdo_empty[2], sdp, p_ready, dq_full, dq_free, acc,
+  // stg (the compute warps' rendezvous around the dQ staging tile)
+  static constexpr int bKv = 0, bQdo = 1, bQdoEmpty = 3, bSdp = 5, bPReady = 6, bDqFull = 7,
+                       bDqFree = 8, bAcc = 9, bStg = 10, kNumBars = 11;
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // 1 KB of slack re-aligns the base to the 128-byte swizzle's 1 KB period;
+  // when it does not fit (d = 128) the kernel requires an aligned base.
+  static constexpr int kSlack = (kBytes + 1024 <= 232448) ? 1024 : 0;
+  static constexpr int kAlloc = kBytes + kSlack;
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr int stage(int s) { return kStage + (s % kStages) * kStageBytes; }
 };
 
 // The CTA's key block and the query blocks it visits.
@@ -118,23 +135,30 @@ __device__ __forceinline__ void bwd_load_role(const CUtensorMap* tm_q, const CUt
   for (; s < wk.steps; ++s) {
     const int h = wk.g * p.group + s / per_head;
     const int qb = wk.qb0 + s % per_head;
-    if (s > 0 && !(ok = w.wait_warp(bar(L::bQdoEmpty), static_cast<uint32_t>(s - 1) & 1u, L::bQdoEmpty)))
+    const int st = s % L::kStages;
+    const uint32_t stg = sbase + L::stage(s);
+    // the stage's previous step (s - kStages) must be done with it
+    if (s >= L::kStages &&
+        !(ok = w.wait_warp(bar(L::bQdoEmpty + st), static_cast<uint32_t>(s / L::kStages - 1) & 1u,
+                           L::bQdoEmpty + st)))
       break;
-    mbar_arrive_expect_tx_warp(bar(L::bQdo), 2u * L::kTileBytes + 1024u);
+    mbar_arrive_expect_tx_warp(bar(L::bQdo + st), 2u * L::kTileBytes + 1024u);
 #pragma unroll
     for (int pn = 0; pn < L::kPanels; ++pn) {
-      tma_load_4d_warp(sbase + L::kQ + pn * L::kPanelBytes, tm_q, bar(L::bQdo), pn * 64, h, qb * 128, wk.b);
-      tma_load_4d_warp(sbase + L::kDO + pn * L::kPanelBytes, tm_do, bar(L::bQdo), pn * 64, h, qb * 128,
+      tma_load_4d_warp(stg + L::kQ + pn * L::kPanelBytes, tm_q, bar(L::bQdo + st), pn * 64, h, qb * 128, wk.b);
+      tma_load_4d_warp(stg + L::kDO + pn * L::kPanelBytes, tm_do, bar(L::bQdo + st), pn * 64, h, qb * 128,
                        wk.b);
     }
     const int64_t row0 = (static_cast<int64_t>(wk.b) * p.Hq + h) * p.Sq_pad + qb * 128;
-    bulk_load_warp(sbase + L::kLse, p.lse2 + row0, 512u, bar(L::bQdo));
-    bulk_load_warp(sbase + L::kDelta, p.delta + row0, 512u, bar(L::bQdo));
+    bulk_load_warp(stg + L::kLse, p.lse2 + row0, 512u, bar(L::bQdo + st));
+    bulk_load_warp(stg + L::kDelta, p.delta + row0, 512u, bar(L::bQdo + st));
   }
   if (__any_sync(0xffffffffu, !ok || *w.abort)) {
     // Let the copies this warp started land before the CTA exits.
     w.drain_warp(bar(L::bKv), 0u, L::bKv);
-    if (s > 0) w.drain_warp(bar(L::bQdo), static_cast<uint32_t>(s - 1) & 1u, L::bQdo);
+    for (int t = max(0, s - L::kStages); t < s; ++t)
+      w.drain_warp(bar(L::bQdo + t % L::kStages), static_cast<uint32_t>(t / L::kStages) & 1u,
+                   L::bQdo + t % L::kStages);
   }
 }
 
@@ -152,15 +176,19 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
   constexpr uint32_t kHi = desc_hi_sw128(1024);
   // K-major views (LBO unused) and MN-major views (LBO = 64-column panel stride).
   const uint32_t k_lo = desc_lo_sw128(sbase + L::kK, 16), v_lo = desc_lo_sw128(sbase + L::kV, 16);
-  const uint32_t q_lo = desc_lo_sw128(sbase + L::kQ, 16), do_lo = desc_lo_sw128(sbase + L::kDO, 16);
-  const uint32_t q_mn = desc_lo_sw128(sbase + L::kQ, L::kPanelBytes);
-  const uint32_t do_mn = desc_lo_sw128(sbase + L::kDO, L::kPanelBytes);
   const uint32_t k_mn = desc_lo_sw128(sbase + L::kK, L::kPanelBytes);
+  constexpr uint32_t kStageStep = L::kStageBytes >> 4;   // descriptor units between stages
   const uint32_t ds_mn = desc_lo_sw128(sbase + L::kDS, L::kPanelBytes);
   bool ok = w.wait_warp(bar(L::bKv), 0u, L::bKv);
   tc_fence_after_sync();
   for (int s = 0; ok && s < wk.steps; ++s) {
-    if (!(ok = w.wait_warp(bar(L::bQdo), static_cast<uint32_t>(s) & 1u, L::bQdo))) break;
+    const int st = s % L::kStages;
+    const uint32_t q_lo = desc_lo_sw128(sbase + L::stage(0) + L::kQ, 16) + st * kStageStep;
+    const uint32_t do_lo = desc_lo_sw128(sbase + L::stage(0) + L::kDO, 16) + st * kStageStep;
+    const uint32_t q_mn = desc_lo_sw128(sbase + L::stage(0) + L::kQ, L::kPanelBytes) + st * kStageStep;
+    const uint32_t do_mn = desc_lo_sw128(sbase + L::stage(0) + L::kDO, L::kPanelBytes) + st * kStageStep;
+    if (!(ok = w.wait_warp(bar(L::bQdo + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bQdo + st)))
+      break;
     if (s > 0 && !(ok = w.wait_warp(bar(L::bDqFree), static_cast<uint32_t>(s - 1) & 1u, L::bDqFree)))
       break;
     tc_fence_after_sync();
@@ -179,16 +207,17 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
     if (!(ok = w.wait_warp(bar(L::bPReady), static_cast<uint32_t>(s) & 1u, L::bPReady))) break;
     tc_fence_after_sync();
     // dV += P^T dO and dK += dS^T Q: 16 queries (8 TMEM columns of packed
-    // BF16, 2 KB of the MN-major operand) per MMA
+    // BF16 -- queries 32 j .. 32 j + 31 at columns 32 j .. 32 j + 15 -- and
+    // 2 KB of the MN-major operand) per MMA
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts_lohi_warp(tmem + L::kColDV, tmem + L::kColS + kk * 8, do_mn + kk * (2048 >> 4), kHi, kIdescTs,
-                       (s > 0 || kk > 0) ? 1u : 0u);
+      mma_ts_lohi_warp(tmem + L::kColDV, tmem + L::kColS + 32 * (kk >> 1) + 8 * (kk & 1),
+                       do_mn + kk * (2048 >> 4), kHi, kIdescTs, (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts_lohi_warp(tmem + L::kColDK, tmem + L::kColDP + kk * 8, q_mn + kk * (2048 >> 4), kHi, kIdescTs,
-                       (s > 0 || kk > 0) ? 1u : 0u);
-    mma_commit_warp(bar(L::bQdoEmpty));
+      mma_ts_lohi_warp(tmem + L::kColDK, tmem + L::kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
+                       q_mn + kk * (2048 >> 4), kHi, kIdescTs, (s > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_warp(bar(L::bQdoEmpty + st));
     // dQ = dS K over the S^T columns: issued after the dV MMA that reads
     // P^T there (one issuing thread's MMAs execute in order)
 #pragma unroll
@@ -203,33 +232,44 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
   w.drain_warp(bar(L::bAcc), 0u, L::bAcc);
 }
 
-// ------------------------------------------------------------ softmax-side WG
+// ------------------------------------------------------------ compute warps
+// Warps 0-7: warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter)
+// and query columns 64 (w / 4) .. + 63 of each step. Per step it forms P^T
+// and dS^T for its 32 x 64 entries, then reads out its half of the step's
+// dQ rows (lanes = queries, columns (w / 4) D/2 .. + D/2) and adds them to
+// the global accumulator; at the end it writes its half of dK and dV.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void bwd_softmax_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                                                 const BwdParams& p, const Waiter& w) {
+__device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint32_t sbase,
+                                                 uint8_t* smem, uint32_t tmem, const BwdParams& p,
+                                                 const Waiter& w) {
   using L = BwdSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = warp * 32 + lane;                       // key row of the block = TMEM lane
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int wq = warp & 3, ch = warp >> 2;             // lane quarter, column half
+  const int r = wq * 32 + lane;                         // key row (and dQ query row) = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const BwdWork wk = bwd_work<CAUSAL>(p);
   const int kabs = wk.k0 + r;
-  const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
-  const float* delta_s = reinterpret_cast<const float*>(smem + L::kDelta);
   const float c2 = p.scale_log2;
   const int shift = p.Sk - p.Sq;
   const int per_head = wk.n_qb - wk.qb0;
+  const bool row_live = kabs < p.Sk;
   bool ok = true;
   for (int s = 0; s < wk.steps; ++s) {
+    const int h = wk.g * p.group + s / per_head;
     const int q0 = (wk.qb0 + s % per_head) * 128;
-    if (!(ok = w.wait(bar(L::bQdo), static_cast<uint32_t>(s) & 1u, L::bQdo))) break;
+    const int st = s % L::kStages;
+    const float4* lse4 = reinterpret_cast<const float4*>(smem + L::stage(s) + L::kLse);
+    const float4* delta4 = reinterpret_cast<const float4*>(smem + L::stage(s) + L::kDelta);
+    if (!(ok = w.wait(bar(L::bQdo + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bQdo + st)))
+      break;
     if (!(ok = w.wait(bar(L::bSdp), static_cast<uint32_t>(s) & 1u, L::bSdp))) break;
     tc_fence_after_sync();
-    // whole block visible to this key row (tile-uniform tests keep the mask off the common path)
-    const bool row_live = kabs < p.Sk;
+    // tile-uniform: every (key, query) pair of the step is visible
     const bool all_visible = !CAUSAL || (wk.k0 + 127 <= q0 + shift);
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * ch + cc;                        // 32-query chunk of the step
       uint32_t sv[32], dv[32];
       tmem_ld_x32(lane_base + L::kColS + 32 * c, sv);
       tmem_ld_x32(lane_base + L::kColDP + 32 * c, dv);
@@ -237,20 +277,29 @@ __device__ __forceinline__ void bwd_softmax_role(uint32_t sbase, uint8_t* smem, 
       tmem_wait_ld_x32(dv);
       uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const int qi = 32 * c + e;
-        float p0 = ex2_mufu(__uint_as_float(sv[e]) * c2 - lse_s[qi]);
-        float p1 = ex2_mufu(__uint_as_float(sv[e + 1]) * c2 - lse_s[qi + 1]);
-        if (!row_live || (!all_visible && kabs > q0 + qi + shift)) p0 = 0.0f;
-        if (!row_live || (!all_visible && kabs > q0 + qi + 1 + shift)) p1 = 0.0f;
-        const float d0 = p0 * (__uint_as_float(dv[e]) - delta_s[qi]);
-        const float d1 = p1 * (__uint_as_float(dv[e + 1]) - delta_s[qi + 1]);
-        pk[e >> 1] = pack_bf16x2(p0, p1);
-        dk[e >> 1] = pack_bf16x2(d0, d1);
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 l4 = lse4[8 * c + e4];
+        const float4 d4 = delta4[8 * c + e4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pe[4], de[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * e4 + u;
+          float pv = ex2_mufu(__uint_as_float(sv[e]) * c2 - lv[u]);
+          if (!row_live || (!all_visible && kabs > q0 + 32 * c + e + shift)) pv = 0.0f;
+          pe[u] = pv;
+          de[u] = pv * (__uint_as_float(dv[e]) - dl[u]);
+        }
+        pk[2 * e4] = pack_bf16x2(pe[0], pe[1]);
+        pk[2 * e4 + 1] = pack_bf16x2(pe[2], pe[3]);
+        dk[2 * e4] = pack_bf16x2(de[0], de[1]);
+        dk[2 * e4 + 1] = pack_bf16x2(de[2], de[3]);
       }
-      // P^T over S^T, dS^T over dP^T (columns already read)
-      tmem_st_x16(lane_base + L::kColS + 16 * c, pk);
-      tmem_st_x16(lane_base + L::kColDP + 16 * c, dk);
+      // P^T over S^T and dS^T over dP^T, in the first 16 of this chunk's own
+      // 32 columns (already read; the other warp of the lane quarter works
+      // on other columns): query q sits at column 32 (q / 32) + (q % 32) / 2
+      tmem_st_x16(lane_base + L::kColS + 32 * c, pk);
+      tmem_st_x16(lane_base + L::kColDP + 32 * c, dk);
       // dS for the dQ MMA: MN-major A tile, panel = 64 queries, row = key,
       // 128-byte swizzle (16-byte chunk index XOR row within its 8-row group)
 #pragma unroll
@@ -267,23 +316,70 @@ __device__ __forceinline__ void bwd_softmax_role(uint32_t sbase, uint8_t* smem, 
     fence_proxy_async_smem();
     tc_fence_before_sync();
     mbar_arrive(bar(L::bPReady));
+    // ---- this step's dQ: half of the columns of the lane quarter's rows
+    if (!(ok = w.wait(bar(L::bDqFull), static_cast<uint32_t>(s) & 1u, L::bDqFull))) break;
+    tc_fence_after_sync();
+    constexpr int kHalf = D / 2;
+    uint32_t x[kHalf];
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c)
+      tmem_ld_x32(lane_base + L::kColS + ch * kHalf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+    // dQ is in registers: the next step's S^T may overwrite its columns
+    tc_fence_before_sync();
+    mbar_arrive(bar(L::bDqFree));
+    // Stage scale * dQ in shared memory (once the previous step's bulk
+    // reduce has read it) and add the 128-row tile to the global
+    // accumulator with one bulk reduce per 32 columns; rows past Sq are
+    // outside the tensor and skipped by the copy.
+    // (rendezvous of the 256 compute threads on an mbarrier, so that a
+    // thread that gives up on a wait cannot leave the others blocked)
+    if (threadIdx.x == 0 && s > 0) bulk_wait_group_read0();
+    mbar_arrive(bar(L::bStg));
+    if (!(ok = w.wait(bar(L::bStg), static_cast<uint32_t>(2 * s) & 1u, L::bStg))) break;
+#pragma unroll
+    for (int cl = 0; cl < kHalf / 32; ++cl) {
+      const int c = ch * (kHalf / 32) + cl;             // 32-column block of the D columns
+      const uint32_t blk = sbase + L::kDqStage + c * 16384 + r * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t addr = blk + (static_cast<uint32_t>(j ^ (r & 7)) << 4);
+        const int e = 32 * cl + 4 * j;
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "f"(__uint_as_float(x[e]) * p.scale), "f"(__uint_as_float(x[e + 1]) * p.scale),
+                     "f"(__uint_as_float(x[e + 2]) * p.scale), "f"(__uint_as_float(x[e + 3]) * p.scale)
+                     : "memory");
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar(L::bStg));
+    if (!(ok = w.wait(bar(L::bStg), static_cast<uint32_t>(2 * s + 1) & 1u, L::bStg))) break;
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+        tma_reduce_add_4d(tm_dq, sbase + L::kDqStage + c * 16384, 32 * c, h, q0, wk.b);
+      bulk_commit_group();
+    }
   }
-  // ---- epilogue: dV, scale * dK -> BF16 -> global
-  const bool row_ok = kabs < p.Sk;
+  // the accumulator must hold every reduce before the CTA exits
+  if (threadIdx.x == 0) bulk_wait_group0();
+  // ---- epilogue: this warp's half of dV and scale * dK -> BF16 -> global
+  constexpr int kHalf = D / 2;
   const int64_t orow = (static_cast<int64_t>(wk.b) * p.Sk + kabs) * p.Hkv + wk.g;
-  __nv_bfloat16* dv_row = p.dv + orow * D;
-  __nv_bfloat16* dk_row = p.dk + orow * D;
+  __nv_bfloat16* dv_row = p.dv + orow * D + ch * kHalf;
+  __nv_bfloat16* dk_row = p.dk + orow * D + ch * kHalf;
   if (ok && wk.steps > 0) {
     if (!w.wait(bar(L::bAcc), 0u, L::bAcc)) return;
     tc_fence_after_sync();
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < kHalf / 32; ++c) {
       uint32_t x[32], y[32];
-      tmem_ld_x32(lane_base + L::kColDV + 32 * c, x);
-      tmem_ld_x32(lane_base + L::kColDK + 32 * c, y);
+      tmem_ld_x32(lane_base + L::kColDV + ch * kHalf + 32 * c, x);
+      tmem_ld_x32(lane_base + L::kColDK + ch * kHalf + 32 * c, y);
       tmem_wait_ld_x32(x);
       tmem_wait_ld_x32(y);
-      if (row_ok) {
+      if (row_live) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 a, b;
@@ -300,47 +396,12 @@ __device__ __forceinline__ void bwd_softmax_role(uint32_t sbase, uint8_t* smem, 
         }
       }
     }
-  } else if (ok && row_ok) {
+  } else if (ok && row_live) {
     // no query reads this key block: zero gradients
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
+    for (int i = 0; i < kHalf / 8; ++i) {
       reinterpret_cast<uint4*>(dv_row)[i] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(dk_row)[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-}
-
-// ------------------------------------------------------------ dQ read-out WG
-template <int D, bool CAUSAL>
-__device__ __forceinline__ void bwd_dq_role(uint32_t sbase, uint32_t tmem, const BwdParams& p,
-                                            const Waiter& w) {
-  using L = BwdSmem<D>;
-  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  const int r = wq * 32 + lane;                         // query row of the block = TMEM lane
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const BwdWork wk = bwd_work<CAUSAL>(p);
-  const int per_head = wk.n_qb - wk.qb0;
-  for (int s = 0; s < wk.steps; ++s) {
-    const int h = wk.g * p.group + s / per_head;
-    const int row = (wk.qb0 + s % per_head) * 128 + r;
-    if (!w.wait(bar(L::bDqFull), static_cast<uint32_t>(s) & 1u, L::bDqFull)) return;
-    tc_fence_after_sync();
-    uint32_t x[D];
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c)
-      tmem_ld_x32(lane_base + L::kColS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
-    // dQ is in registers: the next step's S^T may overwrite its columns
-    tc_fence_before_sync();
-    mbar_arrive(bar(L::bDqFree));
-    if (row < p.Sq) {
-      float* dst = p.dq_acc + ((static_cast<int64_t>(wk.b) * p.Sq + row) * p.Hq + h) * D;
-#pragma unroll
-      for (int e = 0; e < D; e += 4)
-        red_add_v4(dst + e, __uint_as_float(x[e]) * p.scale, __uint_as_float(x[e + 1]) * p.scale,
-                   __uint_as_float(x[e + 2]) * p.scale, __uint_as_float(x[e + 3]) * p.scale);
     }
   }
 }
@@ -350,9 +411,14 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa4_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
+  if (L::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+    // no room to re-align: refuse rather than touch memory past the allocation
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, kStatusMisalignedSmem);
+    return;
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -368,12 +434,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 1 && lane == 0) {
     mbar_init(bar(L::bKv), 1);
     mbar_init(bar(L::bQdo), 1);
+    mbar_init(bar(L::bQdo + 1), 1);
     mbar_init(bar(L::bQdoEmpty), 1);
+    mbar_init(bar(L::bQdoEmpty + 1), 1);
     mbar_init(bar(L::bSdp), 1);
-    mbar_init(bar(L::bPReady), 128);
+    mbar_init(bar(L::bPReady), 256);
     mbar_init(bar(L::bDqFull), 1);
-    mbar_init(bar(L::bDqFree), 128);
+    mbar_init(bar(L::bDqFree), 256);
     mbar_init(bar(L::bAcc), 1);
+    mbar_init(bar(L::bStg), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -382,18 +451,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 8) {
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    bwd_softmax_role<D, CAUSAL>(sbase, smem, tmem, p, w);
-  } else if (warp < 8) {
-    const Waiter w{abort_flag, p.status, kRoleCorrection};
-    bwd_dq_role<D, CAUSAL>(sbase, tmem, p, w);
+    bwd_compute_role<D, CAUSAL>(&tm_dq, sbase, smem, tmem, p, w);
   } else if (warp == kBwdWarpLoad) {
     const Waiter w{abort_flag, p.status, kRoleLoad};
     bwd_load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, &tm_do, sbase, p, w);

@@ -27,7 +27,8 @@ FA4_DECLARE_LAUNCH(launch_fwd_d128_traced)
 // Attention backward (fa4_bwd.cu): zero dq_acc, preprocess (lse2, delta),
 // main kernel (dK, dV, atomic dQ), dq_acc -> dq.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
+                       const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
                        float* dq_acc, float* lse2, float* delta, int B, int Hq, int Hkv, int Sq,
                        int Sk, int d, float scale, bool causal, unsigned int* status,
