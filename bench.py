@@ -36,6 +36,9 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of 2.25 PFLOP/s roofline"
+METRIC_BWD = ("attention bwd TFLOP/s (2.5 x forward FLOPs: five products) on 1 GB300 (BF16) "
+              "and % of 2.25 PFLOP/s roofline")
+BWD_FLOP_FACTOR = 2.5
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_NAME = "fa4_fwd_kernel"
@@ -195,6 +198,24 @@ def oracle_rate(w: workloads.Workload, q, k, v, seconds: float, seed: int = 0
     return f / dt, f, oracle.num_threads(), f"{n} seeded random query rows of {total_rows}"
 
 
+def oracle_bwd_rate(w: workloads.Workload, q, k, v, seed: int = 0) -> Tuple[float, int, str]:
+    """Time the fp64 backward reference on one (batch, query head) of the
+    workload -- the smallest piece it computes whole -- with a seeded dO;
+    returns (flop/s credited at 2.5x the forward FLOPs of that head, threads,
+    sample)."""
+    import torch
+    from oracle import attn_bwd as ob
+    kv = w.Hq // w.Hkv
+    q1 = q[:1, :, :1].contiguous()
+    k1, v1 = k[:1, :, :1].contiguous(), v[:1, :, :1].contiguous()
+    do1 = torch.randn(q1.shape, generator=torch.Generator().manual_seed(seed + 77)).to(torch.bfloat16)
+    t = time.perf_counter()
+    ob.attention_bwd(q1, k1, v1, do1, w.scale, w.causal)
+    dt = time.perf_counter() - t
+    f = BWD_FLOP_FACTOR * w.flops / (w.B * w.Hq)
+    return f / dt, torch.get_num_threads(), f"one (batch, head) of {w.B * w.Hq} (kv group {kv})"
+
+
 def run_reference(args, w: workloads.Workload) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
@@ -262,8 +283,24 @@ def run_ours(args, w: workloads.Workload) -> None:
                                                                     args.num_splits),
                                         dtype=torch.uint8, device=dev))
 
+    bwd = args.pass_ == "bwd"
+    if bwd:
+        # the backward's inputs: the forward's outputs and a seeded dO
+        fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream)
+        g = torch.Generator().manual_seed(7 + batch_offset)
+        do_h = torch.randn(q_h.shape, generator=g).to(torch.bfloat16)
+        dout = do_h.to(dev)
+        o_h, lse_h = o.cpu(), lse.cpu()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsb = torch.empty(fa4.bwd_workspace_bytes(w_rank.B, w.Hq, w.Sq, w.d), dtype=torch.uint8,
+                          device=dev)
+
     def launch():
-        fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
+        if bwd:
+            fa4.bwd_into(q, k, v, o, dout, lse, dq, dk, dv, w.causal, w.scale, workspace=wsb,
+                         stream=stream)
+        else:
+            fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -304,6 +341,11 @@ def run_ours(args, w: workloads.Workload) -> None:
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     o_p = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     lse_p = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    if bwd:
+        o_bp, lse_bp, do_p = o_h.pin_memory(), lse_h.pin_memory(), do_h.pin_memory()
+        dq_p = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+        dk_p = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
+        dv_p = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -316,42 +358,58 @@ def run_ours(args, w: workloads.Workload) -> None:
             q.copy_(q_p, non_blocking=True)
             k.copy_(k_p, non_blocking=True)
             v.copy_(v_p, non_blocking=True)
+            if bwd:
+                o.copy_(o_bp, non_blocking=True)
+                lse.copy_(lse_bp, non_blocking=True)
+                dout.copy_(do_p, non_blocking=True)
             launch()
-            o_p.copy_(o, non_blocking=True)
-            lse_p.copy_(lse, non_blocking=True)
+            if bwd:
+                dq_p.copy_(dq, non_blocking=True)
+                dk_p.copy_(dk, non_blocking=True)
+                dv_p.copy_(dv, non_blocking=True)
+            else:
+                o_p.copy_(o, non_blocking=True)
+                lse_p.copy_(lse, non_blocking=True)
         e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end)
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2 + lse.numel() * 4
+    if bwd:
+        h2d += o.numel() * 2 + lse.numel() * 4 + dout.numel() * 2
+        d2h = (dq.numel() + dk.numel() + dv.numel()) * 2
 
     if pg:
         kernel_ms, e2e_ms = max_over_ranks([kernel_ms, e2e_ms], pg, dev)
 
-    flops_rank_step = w_rank.flops
+    flops_rank_step = w_rank.flops * (BWD_FLOP_FACTOR if bwd else 1.0)
     value = flops_rank_step * args.steps * world / (kernel_ms * 1e-3) / 1e12
     e2e_value = flops_rank_step * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
     per_launch_ms = kernel_ms / args.steps
     achieved = flops_rank_step / (per_launch_ms * 1e-3) / 1e12
     peaks = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
-    traffic = stored_traffic(w.name)
+    traffic = None if bwd else stored_traffic(w.name)
 
     if rank == 0:
         cpu = None
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and bwd:
+            rate, threads, sample = oracle_bwd_rate(w, q_h, k_h, v_h)
+            cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": sample}
+        elif world == 1 and not args.no_cpu_baseline:
             rate, _, threads, sample = oracle_rate(w, q_h, k_h, v_h, args.cpu_seconds)
             cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": sample}
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_launch_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": dict(w.describe(), global_batch=w.B * world, parallelism=f"replica-shards{world}",
                            l2="flushed before every timed launch (256 MiB write)",
                            tau=args.tau, exp2_emulation=args.exp2_emulation,
-                           num_splits=args.num_splits),
+                           num_splits=args.num_splits, **{"pass": args.pass_}),
             "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
@@ -363,7 +421,7 @@ def run_ours(args, w: workloads.Workload) -> None:
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps * (2 if args.num_splits else 1),
+            "gpu_launches": args.steps * (3 if bwd else (2 if args.num_splits else 1)),
         }
         print(json.dumps(line), flush=True)
     if pg:
@@ -380,6 +438,8 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--workload", default=workloads.LONG_CAUSAL.name,
                     choices=[x.name for x in workloads.ALL_NAMED])
     ap.add_argument("--tau", type=float, default=8.0)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward (dQ, dK, dV)")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="key-range split forward with this many splits (0: plain forward)")
     ap.add_argument("--exp2-emulation", type=int, choices=[0, 4, 8], default=0,
