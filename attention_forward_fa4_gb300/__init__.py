@@ -91,6 +91,9 @@ def load_library():
     lib.fa4_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                             vp, ctypes.c_uint64, vp]
     lib.fa4_bwd.restype = i32
+    lib.fa4_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                               i32, i32, vp, ctypes.c_uint64, vp]
+    lib.fa4_bwd_ex.restype = i32
     lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa4_fwd_default_options.restype = None
     lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
@@ -234,7 +237,7 @@ def bwd_workspace_bytes(B: int, Hq: int, Sq: int, d: int) -> int:
 def bwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              dout: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
              dv: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
-             workspace: Optional[torch.Tensor] = None,
+             deterministic: bool = False, workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> None:
     """``fa4_bwd``: write dq, dk, dv (preallocated, BF16) for the upstream
     gradient ``dout``; ``o`` and ``lse`` are the forward's outputs.
@@ -260,11 +263,11 @@ def bwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
-    code = lib.fa4_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq,
-                       Sk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
-                       workspace.numel(), _stream_handle(stream))
-    _check(code, "fa4_bwd")
+    code = lib.fa4_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv,
+                          Sq, Sk, d, float(scale), int(bool(causal)), int(bool(deterministic)),
+                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(code, "fa4_bwd_ex")
 
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,

@@ -365,14 +365,24 @@ uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_s
 uint64_t fa4_bwd_workspace_bytes(int B, int Hq, int Sq, int d) {
   if (B < 0 || Hq < 0 || Sq < 0 || d < 0) return 0;
   const uint64_t sq_pad = (static_cast<uint64_t>(Sq) + 127) / 128 * 128;
-  return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4;
+  const uint64_t turns = (static_cast<uint64_t>(B) * Hq * (sq_pad / 128) * 4 + 15) / 16 * 16;
+  return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4 + turns;
 }
 
 fa4_status fa4_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                    const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
                    int Sk, int d, float scale, int causal, void* workspace,
                    uint64_t workspace_bytes, fa4_stream_t stream) {
+  return fa4_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, scale, causal, 0,
+                    workspace, workspace_bytes, stream);
+}
+
+fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                      int Sq, int Sk, int d, float scale, int causal, int deterministic,
+                      void* workspace, uint64_t workspace_bytes, fa4_stream_t stream) {
   using namespace fa4;
+  if (deterministic != 0 && deterministic != 1) return FA4_ERR_INVALID_ARG;
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return FA4_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA4_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA4_ERR_INVALID_ARG;
@@ -435,11 +445,13 @@ fa4_status fa4_bwd(const void* q, const void* k, const void* v, const void* o, c
     return FA4_ERR_CUDA;
   float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
   float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);
+  int* turns = reinterpret_cast<int*>(delta + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128));
   cudaError_t err = launch_bwd(tq, tk, tv, tdo, tdq, static_cast<const __nv_bfloat16*>(o),
                                static_cast<const __nv_bfloat16*>(dout), lse,
                                static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                               static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta, B, Hq, Hkv, Sq,
-                               Sk, d, scale, causal != 0, status, s);
+                               static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta,
+                               deterministic ? turns : nullptr, B, Hq, Hkv, Sq, Sk, d, scale,
+                               causal != 0, status, s);
   return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
 }
 

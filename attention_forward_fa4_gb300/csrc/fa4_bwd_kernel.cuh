@@ -28,9 +28,10 @@
 // LSE2 = LSE log2(e) (+inf for rows that must contribute nothing) come from
 // a preprocessing kernel, padded to whole 128-row blocks.
 //
-// Warps: 0-7 softmax-side work, dQ read-out and atomics, and the dK/dV
+// Warps: 0-7 softmax-side work, dQ read-out and staging, and the dK/dV
 // epilogue (two warps per TMEM lane quarter, each on half of the columns);
-// 8 TMA loads, 9 MMA issue (both warp-wide with an elected lane); 10-11
+// 8 TMA loads, 9 MMA issue (both warp-wide with an elected lane); 10 dQ
+// flush (bulk reduce-adds; in deterministic mode in key-block order); 11
 // idle. Every wait is bounded (Waiter), as in the forward kernel.
 #pragma once
 
@@ -41,6 +42,7 @@ namespace fa4 {
 constexpr int kBwdThreads = 384;
 constexpr int kBwdWarpLoad = 8;
 constexpr int kBwdWarpMma = 9;
+constexpr int kBwdWarpFlush = 10;
 
 struct BwdParams {
   __nv_bfloat16* dk;        // [B, Sk, Hkv, D]
@@ -51,6 +53,11 @@ struct BwdParams {
   int B, Hq, Hkv, Sq, Sk, group, Sq_pad, n_kblk;
   float scale, scale_log2;
   unsigned int* status;
+  // Deterministic mode (non-null): one int per (batch, query head, query
+  // block), zeroed; the dQ tile of key block kb is added only once kb
+  // earlier key blocks have added theirs, so the fp32 sums are formed in
+  // the same order on every run. CTAs are then numbered key block first.
+  int* dq_turn;
 };
 
 // Q, dO, LSE2 and Delta of a step sit in one of kStages stages (two at
@@ -75,7 +82,7 @@ struct BwdSmem {
   // barriers: kv, qdo[2], qdo_empty[2], sdp, p_ready, dq_full, dq_free, acc,
   // stg (the compute warps' rendezvous around the dQ staging tile)
   static constexpr int bKv = 0, bQdo = 1, bQdoEmpty = 3, bSdp = 5, bPReady = 6, bDqFull = 7,
-                       bDqFree = 8, bAcc = 9, bStg = 10, kNumBars = 11;
+                       bDqFree = 8, bAcc = 9, bStgFull = 10, bStgFree = 11, kNumBars = 12;
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   // 1 KB of slack re-aligns the base to the 128-byte swizzle's 1 KB period;
@@ -98,8 +105,12 @@ template <bool CAUSAL>
 __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
   BwdWork w;
   const int id = static_cast<int>(blockIdx.x);
-  const int kb = id % p.n_kblk;
-  const int bg = id / p.n_kblk;
+  // Key blocks of one (batch, kv head) side by side (their CTAs share Q and
+  // dO in L2); in deterministic mode key block first, so every CTA whose
+  // turn comes earlier was dispatched earlier.
+  const int n_bg = p.B * p.Hkv;
+  const int kb = p.dq_turn ? id / n_bg : id % p.n_kblk;
+  const int bg = p.dq_turn ? id % n_bg : id / p.n_kblk;
   w.b = bg / p.Hkv;
   w.g = bg - w.b * p.Hkv;
   w.k0 = kb * 128;
@@ -329,15 +340,11 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
     // dQ is in registers: the next step's S^T may overwrite its columns
     tc_fence_before_sync();
     mbar_arrive(bar(L::bDqFree));
-    // Stage scale * dQ in shared memory (once the previous step's bulk
-    // reduce has read it) and add the 128-row tile to the global
-    // accumulator with one bulk reduce per 32 columns; rows past Sq are
-    // outside the tensor and skipped by the copy.
-    // (rendezvous of the 256 compute threads on an mbarrier, so that a
-    // thread that gives up on a wait cannot leave the others blocked)
-    if (threadIdx.x == 0 && s > 0) bulk_wait_group_read0();
-    mbar_arrive(bar(L::bStg));
-    if (!(ok = w.wait(bar(L::bStg), static_cast<uint32_t>(2 * s) & 1u, L::bStg))) break;
+    // Stage scale * dQ in shared memory once the flush warp has handed the
+    // tile back from the previous step; the flush warp adds it to the
+    // global accumulator.
+    if (s > 0 && !(ok = w.wait(bar(L::bStgFree), static_cast<uint32_t>(s - 1) & 1u, L::bStgFree)))
+      break;
 #pragma unroll
     for (int cl = 0; cl < kHalf / 32; ++cl) {
       const int c = ch * (kHalf / 32) + cl;             // 32-column block of the D columns
@@ -353,17 +360,8 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
       }
     }
     fence_proxy_async_smem();
-    mbar_arrive(bar(L::bStg));
-    if (!(ok = w.wait(bar(L::bStg), static_cast<uint32_t>(2 * s + 1) & 1u, L::bStg))) break;
-    if (threadIdx.x == 0) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-        tma_reduce_add_4d(tm_dq, sbase + L::kDqStage + c * 16384, 32 * c, h, q0, wk.b);
-      bulk_commit_group();
-    }
+    mbar_arrive(bar(L::bStgFull));
   }
-  // the accumulator must hold every reduce before the CTA exits
-  if (threadIdx.x == 0) bulk_wait_group0();
   // ---- epilogue: this warp's half of dV and scale * dK -> BF16 -> global
   constexpr int kHalf = D / 2;
   const int64_t orow = (static_cast<int64_t>(wk.b) * p.Sk + kabs) * p.Hkv + wk.g;
@@ -406,6 +404,74 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
   }
 }
 
+// ------------------------------------------------------------ dQ flush warp
+// Adds each step's staged dQ tile to the global fp32 accumulator with one
+// bulk tensor reduce-add per 32 columns (rows past Sq are outside the
+// tensor and skipped), then hands the tile back once the copies have read
+// it. In deterministic mode it first waits for its turn on the query
+// block's counter and, after the reduce has completed, passes the turn on.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void bwd_flush_role(const CUtensorMap* tm_dq, uint32_t sbase,
+                                               const BwdParams& p, const Waiter& w) {
+  using L = BwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const int per_head = wk.n_qb - wk.qb0;
+  const int lane = threadIdx.x & 31;
+  const int kb = wk.k0 / 128;
+  bool ok = true;
+  for (int s = 0; s < wk.steps; ++s) {
+    const int h = wk.g * p.group + s / per_head;
+    const int qb = wk.qb0 + s % per_head;
+    if (!(ok = w.wait(bar(L::bStgFull), static_cast<uint32_t>(s) & 1u, L::bStgFull))) break;
+    if (lane == 0) {
+      int* turn = p.dq_turn ? p.dq_turn + (static_cast<int64_t>(wk.b) * p.Hq + h) * wk.n_qb + qb : nullptr;
+      if (turn) {
+        // every earlier key block reads this query block (visibility grows
+        // with the key index), so the turn of key block kb comes after kb adds
+        const long long t0 = clock64();
+        while (true) {
+          int cur;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(turn) : "memory");
+          if (cur >= kb) break;
+          if (*w.abort || clock64() - t0 > kWaitLimitCycles) {
+            if (!*w.abort) {
+              *w.abort = 1;
+              if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
+                p.status[1] = kRoleCorrection;
+                p.status[2] = L::bStgFull;
+                p.status[3] = blockIdx.x;
+              }
+            }
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tma_reduce_add_4d(tm_dq, sbase + L::kDqStage + c * 16384, 32 * c, h, qb * 128, wk.b);
+        bulk_commit_group();
+        if (turn) {
+          bulk_wait_group0();                         // the adds are done in global memory
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          atomicAdd(turn, 1);
+        } else {
+          bulk_wait_group_read0();                    // the tile may be rewritten
+        }
+      }
+      mbar_arrive(bar(L::bStgFree));
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+  }
+  // the accumulator must hold every reduce before the CTA exits
+  if (lane == 0) bulk_wait_group0();
+}
+
 // ------------------------------------------------------------ kernel
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -442,7 +508,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bDqFull), 1);
     mbar_init(bar(L::bDqFree), 256);
     mbar_init(bar(L::bAcc), 1);
-    mbar_init(bar(L::bStg), 256);
+    mbar_init(bar(L::bStgFull), 256);
+    mbar_init(bar(L::bStgFree), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -467,6 +534,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdWarpMma) {
     const Waiter w{abort_flag, p.status, kRoleMma};
     bwd_mma_role<D, CAUSAL>(sbase, tmem, p, w);
+  } else if (warp == kBwdWarpFlush) {
+    const Waiter w{abort_flag, p.status, kRoleCorrection};
+    bwd_flush_role<D, CAUSAL>(&tm_dq, sbase, p, w);
   }
 
   tc_fence_before_sync();

@@ -30,9 +30,9 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
                        const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
-                       float* dq_acc, float* lse2, float* delta, int B, int Hq, int Hkv, int Sq,
-                       int Sk, int d, float scale, bool causal, unsigned int* status,
-                       cudaStream_t s);
+                       float* dq_acc, float* lse2, float* delta, int* dq_turn, int B, int Hq,
+                       int Hkv, int Sq, int Sk, int d, float scale, bool causal,
+                       unsigned int* status, cudaStream_t s);
 
 // Largest number of key-range splits fa4_fwd_splitkv accepts.
 constexpr int kMaxSplits = 128;

@@ -151,7 +151,8 @@ fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, floa
  *   workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
  *                    least fa4_bwd_workspace_bytes(B, Hq, Sq, d) bytes: the
  *                    fp32 dQ accumulator [B, Sq, Hq, d], then LSE log2(e)
- *                    and rowsum(dO o O), each [B, Hq, Sq rounded up to 128].
+ *                    and rowsum(dO o O), each [B, Hq, Sq rounded up to 128],
+ *                    then one int per (batch, query head, query block).
  *   other arguments and rules as fa4_fwd; dq, dk, dv and the workspace
  *   must not overlap each other or any input.
  * Enqueues a memset, a preprocessing kernel, the main kernel and a
@@ -163,6 +164,22 @@ fa4_status fa4_bwd(const void *q, const void *k, const void *v, const void *o, c
                    const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
                    int Sq, int Sk, int d, float scale, int causal, void *workspace,
                    uint64_t workspace_bytes, fa4_stream_t stream);
+
+/*
+ * fa4_bwd_ex -- fa4_bwd with deterministic = 0 (the same) or 1: the tiles
+ * of dQ that different key blocks contribute are added to the fp32
+ * accumulator in key-block order (each CTA waits for its turn on a per
+ * query-block counter kept in the workspace), so dq is bit-for-bit the same
+ * on every run ("FlashAttention-4: Algorithm and Kernel Pipelining
+ * Co-Design for Asymmetric Hardware Scaling", §1: a deterministic execution
+ * mode for reproducible training). dk and dv are deterministic in both
+ * modes (each is accumulated inside one CTA).
+ */
+fa4_status fa4_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                      const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                      int deterministic, void *workspace, uint64_t workspace_bytes,
+                      fa4_stream_t stream);
 
 /*
  * fa4_fwd_splitkv -- the same forward, with the keys cut into num_splits

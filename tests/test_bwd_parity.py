@@ -88,3 +88,29 @@ def test_bwd_empty_edges():
     dq, dk, dv = fa4.bwd(q, ke, ke.clone(), o, torch.ones_like(q), lse)
     torch.cuda.synchronize()
     assert (dq == 0).all()
+
+
+@pytest.mark.parametrize("case", [(1, 4, 2, 1024, 2048, 128, True), (2, 2, 2, 700, 900, 64, False)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_deterministic_mode_repeats_bit_for_bit_and_matches_oracle(case):
+    """fa4_bwd_ex(deterministic=1) adds the key blocks' dQ tiles in key-block
+    order: repeated runs agree bit for bit, and the result is the gradient."""
+    fa4 = _fa4()
+    B, Hq, Hkv, Sq, Sk, d, causal = case
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=93)
+    do = torch.randn((B, Sq, Hq, d), generator=torch.Generator().manual_seed(94)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa4.fwd(qd, kd, vd, causal=causal, scale=scale)
+    runs = [fa4.bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, deterministic=True)
+            for _ in range(3)]
+    torch.cuda.synchronize()
+    code, detail = fa4.device_status(clear=True)
+    assert code == fa4.FA4_OK, f"device status {code} {detail}"
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert torch.equal(a, b)
+    ref = ob.attention_bwd(q, k, v, do, scale, causal)
+    log = [str(case)]
+    for name, got in zip(("dq", "dk", "dv"), runs[0]):
+        _check(name, got, ref[name], log)
