@@ -13,4 +13,6 @@ Contents:
                  Horner polynomial) with its own minimax fit.
   splitkv     -- fp64 key-range forward and the LSE-weighted combine.
   attn_bwd    -- fp64 gradient of attention (dQ, dK, dV) by the definition.
+  fp8         -- e4m3 decoding and the fp64 forward of dequantised FP8
+                 inputs, with the error bound of rounding P to e4m3.
 """

@@ -53,3 +53,25 @@ def gather_gpu_rows(o: torch.Tensor, lse: torch.Tensor, rows: torch.Tensor):
     o_r = o[b.to(dev), i.to(dev), h.to(dev), :]
     l_r = lse[b.to(dev), h.to(dev), i.to(dev)]
     return to_np(o_r), to_np(l_r)
+
+
+# FP8 forward: no stated tolerance; derived from the e4m3 rounding of P (see
+# oracle/fp8.py for `bound` and `rss`) plus the BF16 rounding of O
+# (half a BF16 ulp = 2^-8 relative) and an fp32-accumulation floor.
+FP8_ABS_FLOOR = 1e-4
+FP8_RSS_RATIO = 1.0
+
+
+def assert_close_fp8(o_gpu, lse_gpu, o_ref, lse_ref, bound, rss, what: str = ""):
+    """Element-wise worst case, a root-mean-square check against the rss
+    scale, and the LSE check of the BF16 path."""
+    mx, mean, lmx = errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    err = np.abs(np.asarray(o_gpu, dtype=np.float64) - o_ref)
+    out_round = 2.0 ** -8 * np.abs(o_ref)
+    worst = bound + out_round + FP8_ABS_FLOOR
+    over = float((err / worst).max()) if err.size else 0.0
+    ratio = float(np.sqrt(np.mean((err / (rss + out_round + 1e-6)) ** 2))) if err.size else 0.0
+    msg = (f"{what}: O max {mx:.3e} mean {mean:.3e} (worst-case use {over:.3f}, "
+           f"rms/rss {ratio:.3f}), LSE max {lmx:.3e}")
+    assert over <= 1.0 and ratio <= FP8_RSS_RATIO and lmx <= LSE_MAX_ABS, msg
+    return mx, mean, lmx, over, ratio

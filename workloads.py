@@ -116,6 +116,55 @@ def make_inputs(w: Workload, seed: int = 0, *, batch_offset: int = 0
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
+E4M3_MAX = 448.0   # largest finite e4m3 value
+
+
+def quantize_e4m3(x: torch.Tensor) -> Tuple[torch.Tensor, float]:
+    """Per-tensor e4m3 quantisation of an fp32/BF16 tensor for FP8 inputs.
+
+    scale = amax / 448 (amax = largest |x|); codes = round-to-nearest-even
+    of x / scale in torch's float8_e4m3fn conversion. Returns (codes, scale)
+    with x ~ codes * scale.
+    """
+    x = x.to(torch.float32)
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    scale = amax / E4M3_MAX if amax > 0 else 1.0
+    codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return codes, scale
+
+
+def make_inputs_fp8(w: Workload, seed: int = 0, *, batch_offset: int = 0):
+    """FP8 inputs of a head-dim-128 workload: the fp32 draws of
+    ``make_inputs`` (same seed, same order), each tensor quantised with
+    ``quantize_e4m3``. Returns (q8, k8, v8, q_scale, k_scale, v_scale)."""
+    g = torch.Generator().manual_seed(seed + 1000003 * batch_offset)
+    q = torch.randn((w.B, w.Sq, w.Hq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Sk, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Sk, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    if w.ramp != 0.0:
+        q_hat = torch.randn((w.d,), generator=g, dtype=torch.float32)
+        q_hat = q_hat / q_hat.norm()
+        j = torch.arange(w.Sk, dtype=torch.float32).view(1, w.Sk, 1, 1)
+        k = k + w.ramp * j * q_hat.view(1, 1, 1, w.d)
+    (q8, qs), (k8, ks), (v8, vs) = quantize_e4m3(q), quantize_e4m3(k), quantize_e4m3(v)
+    return q8, k8, v8, qs, ks, vs
+
+
+def make_custom_fp8(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int = 128, seed: int = 0,
+                    dist: str = "randn"):
+    """Seeded FP8 inputs of arbitrary shape: ``make_custom``'s draws (before
+    the BF16 rounding) quantised per tensor. Same return as make_inputs_fp8."""
+    g = torch.Generator().manual_seed(seed)
+    mul = 4.0 if dist == "wide" else 1.0
+    if dist not in ("randn", "wide"):
+        raise ValueError(dist)
+    q = mul * torch.randn((B, Sq, Hq, d), generator=g)
+    k = mul * torch.randn((B, Sk, Hkv, d), generator=g)
+    v = torch.randn((B, Sk, Hkv, d), generator=g)
+    (q8, qs), (k8, ks), (v8, vs) = quantize_e4m3(q), quantize_e4m3(k), quantize_e4m3(v)
+    return q8, k8, v8, qs, ks, vs
+
+
 def make_custom(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int, seed: int = 0,
                 dist: str = "randn") -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Seeded BF16 inputs of arbitrary shape for edge-case tests."""
