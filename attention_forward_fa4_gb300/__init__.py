@@ -22,7 +22,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["fwd", "fwd_into", "exp2_eval", "device_status", "status_string", "version",
+__all__ = ["fwd", "fwd_into", "fwd_fp8", "fwd_fp8_into", "exp2_eval", "device_status", "status_string", "version",
            "lib_path", "load_library", "Fa4Error", "FA4_OK", "FA4_ERR_INVALID_ARG",
            "FA4_ERR_UNSUPPORTED", "FA4_ERR_MISALIGNED", "FA4_ERR_CUDA", "FA4_ERR_TIMEOUT"]
 
@@ -76,6 +76,9 @@ def load_library():
     lib.fa4_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                ctypes.POINTER(_Options), vp]
     lib.fa4_fwd_ex.restype = i32
+    lib.fa4_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                f32, f32, f32, vp, vp]
+    lib.fa4_fwd_fp8.restype = i32
     lib.fa4_fwd_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.fa4_fwd_splitkv_workspace_bytes.restype = ctypes.c_uint64
     lib.fa4_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
@@ -277,6 +280,66 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     bwd_into(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, **kw)
     return dq, dk, dv
+
+
+def fwd_fp8_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                 lse: torch.Tensor, q_scale: float, k_scale: float, v_scale: float,
+                 causal: bool = False, scale: Optional[float] = None, *, tau: float = 8.0,
+                 rescale_stats: Optional[torch.Tensor] = None,
+                 strict_mma_order: bool = False, grid_mode: int = 0,
+                 stream: Optional[torch.cuda.Stream] = None) -> None:
+    """FP8 forward (``fa4_fwd_fp8``) into preallocated ``o`` and ``lse``.
+
+    q [B,Sq,Hq,128], k/v [B,Sk,Hkv,128] hold e4m3 codes (torch.float8_e4m3fn,
+    or uint8 bit patterns) whose true values are code * q_scale / k_scale /
+    v_scale; o [B,Sq,Hq,128] BF16 and lse [B,Hq,Sq] fp32 receive the forward
+    of the true values. ``scale`` defaults to 1/sqrt(128).
+    """
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be float8_e4m3fn (or uint8 codes), got {t.dtype}")
+    for name, t, dt in (("o", o, torch.bfloat16), ("lse", lse, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,Sq,Hq,d] and k, v [B,Sk,Hkv,d]")
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("o must match q and lse must be [B,Hq,Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opt = _Options()
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    opt.tau = float(tau)
+    opt.strict_mma_order = 1 if strict_mma_order else 0
+    opt.grid_mode = int(grid_mode)
+    if rescale_stats is not None:
+        if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
+            raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")
+        opt.rescale_stats = rescale_stats.data_ptr()
+    code = lib.fa4_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
+                           float(q_scale), float(k_scale), float(v_scale), ctypes.byref(opt),
+                           _stream_handle(stream))
+    _check(code, "fa4_fwd_fp8")
+
+
+def fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: float, k_scale: float,
+            v_scale: float, causal: bool = False, scale: Optional[float] = None,
+            **kw) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FP8 forward; returns (o [B,Sq,Hq,128] BF16, lse [B,Hq,Sq] fp32)."""
+    B, Sq, Hq, d = q.shape
+    o = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    fwd_fp8_into(q, k, v, o, lse, q_scale, k_scale, v_scale, causal, scale, **kw)
+    return o, lse
 
 
 def splitkv_workspace_bytes(B: int, Hq: int, Sq: int, d: int, num_splits: int) -> int:

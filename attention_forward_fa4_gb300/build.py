@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa4.so")
 
-UNITS = ["fa4_api.cu", "fa4_merge.cu", "fa4_bwd.cu", "fa4_fwd_d64.cu", "fa4_fwd_d128.cu",
-         "fa4_fwd_d64_traced.cu", "fa4_fwd_d128_traced.cu"]
+UNITS = ["fa4_api.cu", "fa4_merge.cu", "fa4_bwd.cu", "fa4_fwd_fp8.cu", "fa4_fwd_d64.cu",
+         "fa4_fwd_d128.cu", "fa4_fwd_d64_traced.cu", "fa4_fwd_d128_traced.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xptxas", "-v", "--expt-relaxed-constexpr",

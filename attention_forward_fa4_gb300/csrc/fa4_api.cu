@@ -109,6 +109,22 @@ bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 [B, S, H, d] tensor as a 4-D map: a 128-column x 128-row box (128
+// one-byte elements = one 128-byte swizzle row).
+bool make_map_u8(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d,
+                                 static_cast<cuuint64_t>(S) * H * d};
+  const cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 [B, S, H, d] tensor (the backward's dQ accumulator) as a 4-D map with
 // a 32-column x 128-row box and 128-byte swizzle (32 fp32 = 128 bytes).
 bool make_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
@@ -203,10 +219,16 @@ namespace {
 // Shared body of fa4_fwd_ex and fa4_fwd_splitkv. With num_splits > 0 the
 // forward runs per key-range split into the workspace and a merge kernel
 // writes o / lse; num_splits == 0 is the plain forward.
+// Dequantisation scales of the FP8 forward (q, k, v hold e4m3 values whose
+// true values are value * scale).
+struct Fp8Scales {
+  float q, k, v;
+};
+
 fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                     int Hkv, int Sq, int Sk, int d, float scale, int causal,
                     const fa4_fwd_options* opt, int num_splits, void* workspace,
-                    size_t workspace_bytes, fa4_stream_t stream) {
+                    size_t workspace_bytes, fa4_stream_t stream, const Fp8Scales* fp8 = nullptr) {
   using namespace fa4;
   fa4_fwd_options o_def;
   fa4_fwd_default_options(&o_def);
@@ -225,6 +247,12 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
+  if (fp8) {
+    auto bad = [](float x) { return !(x > 0.0f) || !std::isfinite(x); };
+    if (bad(fp8->q) || bad(fp8->k) || bad(fp8->v)) return FA4_ERR_INVALID_ARG;
+    // built for head dim 128, all exponentials on MUFU, no trace, no split
+    if (d != 128 || op.exp2_emulation != 0 || op.trace || num_splits != 0) return FA4_ERR_UNSUPPORTED;
+  }
   if (B == 0 || Sq == 0) return FA4_OK;  // empty output: nothing to do
   if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
   auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -235,11 +263,13 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
     return FA4_ERR_MISALIGNED;
   if (op.trace && (reinterpret_cast<uintptr_t>(op.trace) & 7u) != 0) return FA4_ERR_MISALIGNED;
   if (op.trace && op.trace_ctas < 0) return FA4_ERR_INVALID_ARG;
-  const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
-  const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
+  const uint64_t in_elem = fp8 ? 1 : 2;
+  const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * in_elem;
+  const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * in_elem;
+  const uint64_t o_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
   const uint64_t lse_bytes = static_cast<uint64_t>(B) * Hq * Sq * 4;
-  if (overlaps(o, q_bytes, q, q_bytes) || overlaps(o, q_bytes, k, kv_bytes) ||
-      overlaps(o, q_bytes, v, kv_bytes) || overlaps(o, q_bytes, lse, lse_bytes) ||
+  if (overlaps(o, o_bytes, q, q_bytes) || overlaps(o, o_bytes, k, kv_bytes) ||
+      overlaps(o, o_bytes, v, kv_bytes) || overlaps(o, o_bytes, lse, lse_bytes) ||
       overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
       overlaps(lse, lse_bytes, v, kv_bytes))
     return FA4_ERR_INVALID_ARG;
@@ -295,14 +325,14 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (Sk == 0) {  // no keys: O = 0, LSE = -inf
-    no_keys_kernel<<<152, 256, 0, s>>>(static_cast<uint4*>(o), static_cast<int64_t>(q_bytes / 16),
+    no_keys_kernel<<<152, 256, 0, s>>>(static_cast<uint4*>(o), static_cast<int64_t>(o_bytes / 16),
                                        lse, static_cast<int64_t>(lse_bytes / 4));
     return cudaGetLastError() == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
   }
 
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
-      !make_map(&tv, v, B, Sk, Hkv, d))
+  auto map = fp8 ? make_map_u8 : make_map;
+  if (!map(&tq, q, B, Sq, Hq, d) || !map(&tk, k, B, Sk, Hkv, d) || !map(&tv, v, B, Sk, Hkv, d))
     return FA4_ERR_CUDA;
 
   FwdParams p;
@@ -322,7 +352,8 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   // CTA per tile. Non-causal tiles of one head are numbered side by side so
   // their K/V reads meet in L2.
   p.head_chunk = causal ? (persistent ? B * Hq : (B * Hq < 8 ? B * Hq : 8)) : 1;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = (fp8 ? scale * fp8->q * fp8->k : scale) * 1.4426950408889634f;
+  p.out_scale = fp8 ? fp8->v : 1.0f;
   p.tau = op.tau;
   p.stats = op.rescale_stats;
   p.status = status;
@@ -338,7 +369,9 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   const bool traced = op.trace != nullptr;
   auto launch = (d == 64) ? (traced ? launch_fwd_d64_traced : launch_fwd_d64)
                           : (traced ? launch_fwd_d128_traced : launch_fwd_d128);
-  cudaError_t err = launch(tq, tk, tv, p, causal != 0, emu, persistent, static_cast<unsigned>(grid), s);
+  cudaError_t err = fp8 ? launch_fwd_d128_fp8(tq, tk, tv, p, causal != 0, persistent,
+                                              static_cast<unsigned>(grid), s)
+                        : launch(tq, tk, tv, p, causal != 0, emu, persistent, static_cast<unsigned>(grid), s);
   if (err != cudaSuccess) return FA4_ERR_CUDA;
   if (o_part) {
     err = launch_merge_splits(o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, n_splits, B,
@@ -354,6 +387,15 @@ fa4_status fa4_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                       int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
                       const fa4_fwd_options* opt, fa4_stream_t stream) {
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr, 0, stream);
+}
+
+fa4_status fa4_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                       float q_scale, float k_scale, float v_scale, const fa4_fwd_options* opt,
+                       fa4_stream_t stream) {
+  const Fp8Scales sc{q_scale, k_scale, v_scale};
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr, 0, stream,
+                  &sc);
 }
 
 uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_splits) {

@@ -97,6 +97,7 @@ struct FwdParams {
   int split_blocks;
   float* o_part;
   float* lse_part;
+  float out_scale;             // multiplies O in the epilogue (V's dequantisation scale; 1 for BF16)
 };
 
 // ------------------------------------------------------------ cycle trace
@@ -152,12 +153,15 @@ __device__ __forceinline__ void trace_mark_lane0(const FwdParams& p, int ev, int
   if ((threadIdx.x & 31) == 0) trace_mark<TRACE>(p, ev, j, t, iter);
 }
 
-template <int D>
+// FP8: Q, K, V (and P) in e4m3 -- one byte per element, so a d = 128 row is
+// a single 128-byte swizzle panel.
+template <int D, bool FP8 = false>
 struct Smem {
-  static constexpr int kTileBytes = kBM * D * 2;         // one 128 x D BF16 tile
-  static constexpr int kPanelBytes = kBM * 128;          // 128 rows x 128 B (64 columns)
-  static constexpr int kPanels = D / 64;
-  static constexpr int kSlots = (D == 128) ? 4 : 8;      // K/V ring depth
+  static_assert(!FP8 || D == 128, "the FP8 forward is built for head dim 128");
+  static constexpr int kTileBytes = kBM * D * (FP8 ? 1 : 2);  // one 128 x D tile
+  static constexpr int kPanelBytes = kBM * 128;          // 128 rows x 128 B
+  static constexpr int kPanels = FP8 ? 1 : D / 64;
+  static constexpr int kSlots = (D == 128 && !FP8) ? 4 : 8;   // K/V ring depth
   static constexpr int kQ = 0;
   static constexpr int kRing = kQ + 2 * kTileBytes;
   static constexpr int kBars = kRing + kSlots * kTileBytes;
@@ -319,11 +323,11 @@ __device__ __forceinline__ Tile make_tile(const FwdParams& p, int id_split) {
 // Q once per work tile (after the previous tile's S MMAs have released the
 // Q buffers), then K_j, V_j of every key block into the slot ring; the
 // ring's fill counter runs on across work tiles.
-template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE, bool FP8 = false>
 __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                           const CUtensorMap* tm_v, uint32_t sbase,
                                           const FwdParams& p, const Waiter& w) {
-  using L = Smem<D>;
+  using L = Smem<D, FP8>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   int fill = 0;     // K/V copies issued so far (ring position)
   int n_q = 0;      // Q copies issued so far
@@ -388,10 +392,10 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // Phases run on across the CTA's work tiles: the ring position, the count
 // of P*V MMAs per query tile and the count of earlier tiles whose O_t the
 // epilogue has to read before the next tile's first P*V overwrites it.
-template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE, bool FP8 = false>
 __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const FwdParams& p,
                                          const Waiter& w) {
-  using L = Smem<D>;
+  using L = Smem<D, FP8>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major
@@ -408,10 +412,20 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 
   auto issue_s = [&](int t, int slot) {
     const uint32_t k_lo = ring_lo_k + slot * kSlotStep;
+    if constexpr (FP8) {
+      // e4m3: 32 elements (32 bytes of the 128-byte row) per MMA
+      constexpr uint32_t kIdesc8 = idesc_e4m3_f32(kBM, kBN, false, false);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-      mma_ss_lohi_warp(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 32; ++kk) {
+        const uint32_t off = (kk * 32) >> 4;
+        mma_ss_lohi_f8_warp(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdesc8, kk > 0 ? 1u : 0u);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+        mma_ss_lohi_warp(tmem + col_s[t], q_lo[t] + off, kHi, k_lo + off, kHi, kIdescQK, kk > 0 ? 1u : 0u);
+      }
     }
     mma_commit_warp(bar(L::bSFull + t));
   };
@@ -425,12 +439,22 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       if (!w.wait_warp(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
+      if constexpr (FP8) {
+        // 32 keys per step: 8 TMEM columns of packed e4m3 P, 32 rows (4 KB) of V
+        static_assert(FA4_P_SLICES == 1, "the FP8 forward releases P as one block");
+        constexpr uint32_t kIdescPv8 = idesc_e4m3_f32(kBM, D, false, true);
 #pragma unroll
-      for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
-        // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
-        const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
-        mma_ts_lohi_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
-                    kIdescPV, (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 32; ++kk)
+          mma_ts_lohi_f8_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (4096 >> 4), kHi,
+                              kIdescPv8, (!first || kk > 0) ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
+          // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
+          const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
+          mma_ts_lohi_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+                      kIdescPV, (!first || kk > 0) ? 1u : 0u);
+        }
       }
     }
     mma_commit_warp(bar(L::bPvDone + t));
@@ -527,10 +551,10 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 }
 
 // ------------------------------------------------------------ correction WG
-template <int D, bool CAUSAL, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, bool PERSIST, bool TRACE, bool FP8 = false>
 __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                                 const FwdParams& p, const Waiter& w) {
-  using L = Smem<D>;
+  using L = Smem<D, FP8>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
@@ -598,10 +622,10 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE, bool FP8 = false>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const FwdParams& p, const Waiter& w) {
-  using L = Smem<D>;
+  using L = Smem<D, FP8>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
@@ -694,7 +718,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    uint32_t pk[64];
+    // P for the P*V MMA: BF16 pairs (64 columns), or with FP8 e4m3 quads
+    // (32 columns; key 4i + j in byte j of column i), rounded from fp32
+    uint32_t pk[FP8 ? 32 : 64];
 #pragma unroll
     for (int pi = 0; pi < 64; ++pi) {
       const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * pi]), __uint_as_float(s[2 * pi + 1])),
@@ -703,16 +729,28 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
                             ? ex2_emulated2(x)
                             : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
       acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
-      pk[pi] = pack_bf16x2(pp.x, pp.y);
+      if constexpr (FP8) {
+        const uint32_t h = pack_e4m3x2(pp.x, pp.y);
+        pk[pi >> 1] = (pi & 1) ? (pk[pi >> 1] | (h << 16)) : h;
+      } else {
+        pk[pi] = pack_bf16x2(pp.x, pp.y);
+      }
     }
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
+    if constexpr (FP8) {
+      tmem_st_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t));
+    }
     constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
 #pragma unroll
-    for (int half = 0; half < FA4_P_SLICES; ++half) {
+    for (int half = 0; half < (FP8 ? 0 : FA4_P_SLICES); ++half) {
 #pragma unroll
       for (int q = 0; q < kSliceCols / 32; ++q)
         tmem_st_x32(s_addr + half * kSliceCols + q * 32,
-                    *reinterpret_cast<const uint32_t(*)[32]>(&pk[half * kSliceCols + q * 32]));
+                    *reinterpret_cast<const uint32_t(*)[32]>(&pk[(half * kSliceCols + q * 32) % (FP8 ? 32 : 64)]));
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
@@ -738,7 +776,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   // partial buffers instead.
   const bool row_valid = row < p.Sq;
   const bool has_keys = n > 0 && m_ref != -INFINITY;
-  const float inv_l = has_keys ? 1.0f / l : 0.0f;
+  const float inv_l = has_keys ? p.out_scale / l : 0.0f;
   const bool partial = p.o_part != nullptr;
   const int64_t orow_idx = (static_cast<int64_t>(tl.b) * p.Sq + row) * p.Hq + tl.h;
   const int64_t part_off = static_cast<int64_t>(tl.split) * p.B * p.Sq * p.Hq;
@@ -801,11 +839,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 }
 
 // ------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -861,19 +899,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     regs_increase<kRegsSoftmax>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD, PERSIST, TRACE>(warp >> 2, sbase, smem, tmem, p, w);
+    softmax_role<D, CAUSAL, EMU_PAIR_PERIOD, PERSIST, TRACE, FP8>(warp >> 2, sbase, smem, tmem, p, w);
   } else if (warp < 12) {
     regs_decrease<kRegsCorrection>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D, CAUSAL, PERSIST, TRACE>(sbase, smem, tmem, p, w);
+    correction_role<D, CAUSAL, PERSIST, TRACE, FP8>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<kRegsLoadMma>();
     if (warp == kWarpLoad) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      load_role<D, CAUSAL, PERSIST, TRACE>(&tm_q, &tm_k, &tm_v, sbase, p, w);
+      load_role<D, CAUSAL, PERSIST, TRACE, FP8>(&tm_q, &tm_k, &tm_v, sbase, p, w);
     } else if (warp == kWarpMma) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      mma_role<D, CAUSAL, PERSIST, TRACE>(sbase, tmem, p, w);
+      mma_role<D, CAUSAL, PERSIST, TRACE, FP8>(sbase, tmem, p, w);
     }
   }
 

@@ -34,6 +34,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        int Hkv, int Sq, int Sk, int d, float scale, bool causal,
                        unsigned int* status, cudaStream_t s);
 
+// FP8 forward (e4m3 Q, K, V; head dim 128).
+cudaError_t launch_fwd_d128_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdParams& p, bool causal, bool persistent, unsigned grid,
+                                cudaStream_t stream);
+
 // Largest number of key-range splits fa4_fwd_splitkv accepts.
 constexpr int kMaxSplits = 128;
 

@@ -7,11 +7,11 @@
 namespace fa4 {
 namespace detail {
 
-template <int D, bool CAUSAL, int EMU, bool PERSIST, bool TRACE>
+template <int D, bool CAUSAL, int EMU, bool PERSIST, bool TRACE, bool FP8 = false>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, unsigned grid, cudaStream_t stream) {
-  constexpr int kSmem = Smem<D>::kAlloc;
-  auto kernel = fa4_fwd_kernel<D, CAUSAL, EMU, PERSIST, TRACE>;
+  constexpr int kSmem = Smem<D, FP8>::kAlloc;
+  auto kernel = fa4_fwd_kernel<D, CAUSAL, EMU, PERSIST, TRACE, FP8>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
   kernel<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);

@@ -134,6 +134,34 @@ fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, floa
                       int causal, const fa4_fwd_options *opt, fa4_stream_t stream);
 
 /*
+ * fa4_fwd_fp8 -- the same forward with Q, K and V in FP8 (e4m3): both
+ * products run on the tensor cores with 8-bit inputs and an fp32
+ * accumulator, the softmax stays in fp32, P is rounded to e4m3 for the
+ * second product, and O is stored in BF16 ("How FlashAttention 4 Works",
+ * the section on where low precision is safe: Q K^T and P V in FP8,
+ * softmax in FP32, the output in BF16/FP16).
+ *
+ * The inputs are scaled codes: the true values are q * q_scale, k * k_scale
+ * and v * v_scale. The result is the forward of those true values,
+ *     S = scale q_scale k_scale (q k^T),   O = v_scale softmax(S) v,
+ * with LSE the natural-log logsumexp of S.
+ *
+ *   q                [B, Sq, Hq, 128] e4m3 bytes, device, 16-byte aligned
+ *   k, v             [B, Sk, Hkv, 128] e4m3 bytes, device, 16-byte aligned
+ *   o                [B, Sq, Hq, 128] BF16, written
+ *   lse              [B, Hq, Sq] fp32, written
+ *   q_scale, k_scale, v_scale  finite and > 0
+ *   other arguments as fa4_fwd_ex. Only d = 128 is built; options must keep
+ *   exp2_emulation = 0 and trace = NULL.
+ * Returns FA4_ERR_UNSUPPORTED for d != 128 or those options,
+ * FA4_ERR_INVALID_ARG for a bad scale, otherwise as fa4_fwd_ex.
+ */
+fa4_status fa4_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                       int causal, float q_scale, float k_scale, float v_scale,
+                       const fa4_fwd_options *opt, fa4_stream_t stream);
+
+/*
  * fa4_bwd -- attention backward: the gradients of O = softmax(scale QK^T
  * [+causal]) V with respect to q, k, v for an upstream gradient dout
  * ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
