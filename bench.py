@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--tau T] [--exp2-emulation 0|4|8]
+                    [--pass fwd|bwd] [--num-splits S] [--precision bf16|fp8]
 
 One step = one attention forward over the workload's synthetic BF16 input
 (default: B=2, Hq=Hkv=16, Sq=Sk=8192, d=128, causal). ``value`` is the
@@ -38,7 +39,10 @@ import workloads  # noqa: E402
 METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of 2.25 PFLOP/s roofline"
 METRIC_BWD = ("attention bwd TFLOP/s (2.5 x forward FLOPs: five products) on 1 GB300 (BF16) "
               "and % of 2.25 PFLOP/s roofline")
+METRIC_FP8 = ("attention fwd TFLOP/s on 1 GB300 (FP8 e4m3 Q, K, V and P, BF16 O) and % of "
+              "4.5 PFLOP/s roofline")
 BWD_FLOP_FACTOR = 2.5
+FP8_OVER_BF16 = 2.0            # nominal dense FP8 : BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_NAME = "fa4_fwd_kernel"
@@ -171,10 +175,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_rate(w: workloads.Workload, q, k, v, seconds: float, seed: int = 0
-                ) -> Tuple[float, float, int, str]:
+def oracle_rate(w: workloads.Workload, q, k, v, seconds: float, seed: int = 0,
+                scale: Optional[float] = None) -> Tuple[float, float, int, str]:
     """Time the fp64 oracle on a seeded random row sample sized for about
     ``seconds`` of host work; returns (flop/s, flops done, threads, sample)."""
+    scale = w.scale if scale is None else scale
     import numpy as np
     from oracle import attn as oracle
 
@@ -187,12 +192,12 @@ def oracle_rate(w: workloads.Workload, q, k, v, seconds: float, seed: int = 0
     total_rows = w.B * w.Hq * w.Sq
     probe = rng.integers(0, total_rows, size=16, dtype=np.int64)
     t = time.perf_counter()
-    oracle.attention_fwd_rows(q, k, v, w.scale, w.causal, probe)
+    oracle.attention_fwd_rows(q, k, v, scale, w.causal, probe)
     dt = max(time.perf_counter() - t, 1e-4)
     n = int(max(16, min(total_rows, 16 * seconds / dt)))
     rows = np.sort(rng.integers(0, total_rows, size=n, dtype=np.int64))
     t = time.perf_counter()
-    oracle.attention_fwd_rows(q, k, v, w.scale, w.causal, rows)
+    oracle.attention_fwd_rows(q, k, v, scale, w.causal, rows)
     dt = time.perf_counter() - t
     f = flops_of(rows)
     return f / dt, f, oracle.num_threads(), f"{n} seeded random query rows of {total_rows}"
@@ -268,12 +273,20 @@ def run_ours(args, w: workloads.Workload) -> None:
     fa4.load_library()
 
     w_rank, batch_offset = shard_workload(w, rank, world)
-    q_h, k_h, v_h = workloads.make_inputs(w_rank, seed=0, batch_offset=batch_offset)
+    bwd = args.pass_ == "bwd"
+    fp8 = args.precision == "fp8"
+    if fp8 and (bwd or args.num_splits or args.exp2_emulation or w.d != 128):
+        raise SystemExit("--precision fp8 times the plain head-dim-128 forward only")
+    if fp8:
+        q_h, k_h, v_h, qs, ks, vs = workloads.make_inputs_fp8(w_rank, seed=0,
+                                                              batch_offset=batch_offset)
+    else:
+        q_h, k_h, v_h = workloads.make_inputs(w_rank, seed=0, batch_offset=batch_offset)
     stream = torch.cuda.Stream(device=dev)
     q = q_h.to(dev)
     k = k_h.to(dev)
     v = v_h.to(dev)
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     kw = dict(tau=args.tau, exp2_emulation=args.exp2_emulation)
@@ -283,7 +296,6 @@ def run_ours(args, w: workloads.Workload) -> None:
                                                                     args.num_splits),
                                         dtype=torch.uint8, device=dev))
 
-    bwd = args.pass_ == "bwd"
     if bwd:
         # the backward's inputs: the forward's outputs and a seeded dO
         fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream)
@@ -299,6 +311,9 @@ def run_ours(args, w: workloads.Workload) -> None:
         if bwd:
             fa4.bwd_into(q, k, v, o, dout, lse, dq, dk, dv, w.causal, w.scale, workspace=wsb,
                          stream=stream)
+        elif fp8:
+            fa4.fwd_fp8_into(q, k, v, o, lse, qs, ks, vs, w.causal, w.scale, tau=args.tau,
+                             stream=stream)
         else:
             fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, stream=stream, **kw)
 
@@ -373,7 +388,7 @@ def run_ours(args, w: workloads.Workload) -> None:
         e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end)
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
     d2h = o.numel() * 2 + lse.numel() * 4
     if bwd:
         h2d += o.numel() * 2 + lse.numel() * 4 + dout.numel() * 2
@@ -388,8 +403,10 @@ def run_ours(args, w: workloads.Workload) -> None:
     per_launch_ms = kernel_ms / args.steps
     achieved = flops_rank_step / (per_launch_ms * 1e-3) / 1e12
     peaks = measured_peaks()
-    peak = float(peaks.get("bf16_tflops", 1900.0))
-    traffic = None if bwd else stored_traffic(w.name)
+    peak = float(peaks.get("bf16_tflops", 1900.0)) * (FP8_OVER_BF16 if fp8 else 1.0)
+    peak_source = f"{peaks['_source']} bf16_tflops (burst)" + (
+        f" x {FP8_OVER_BF16:g} (nominal FP8:BF16 dense ratio)" if fp8 else "")
+    traffic = None if bwd else stored_traffic(w.name + ("_fp8" if fp8 else ""))
 
     if rank == 0:
         cpu = None
@@ -397,23 +414,39 @@ def run_ours(args, w: workloads.Workload) -> None:
             rate, threads, sample = oracle_bwd_rate(w, q_h, k_h, v_h)
             cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": sample}
+        elif world == 1 and not args.no_cpu_baseline and fp8:
+            # the FP8 oracle's forward equals the fp64 definition on the e4m3
+            # values (exact in BF16) with the scales folded into scale and O
+            from oracle import fp8 as o8
+            deq = [torch.from_numpy(o8.e4m3_to_float(o8.codes_of(t))).to(torch.bfloat16)
+                   for t in (q_h, k_h, v_h)]
+            rate, _, threads, sample = oracle_rate(w, *deq, args.cpu_seconds,
+                                                   scale=w.scale * qs * ks)
+            cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": sample + " (fp64 definition on the dequantised e4m3 inputs)"}
         elif world == 1 and not args.no_cpu_baseline:
             rate, _, threads, sample = oracle_rate(w, q_h, k_h, v_h, args.cpu_seconds)
             cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": sample}
         line = {
-            "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC_BWD if bwd else (METRIC_FP8 if fp8 else METRIC), "value": value,
+            "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_launch_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if fp8 else "bf16",
             "data": "synthetic",
             "config": dict(w.describe(), global_batch=w.B * world, parallelism=f"replica-shards{world}",
+                           **({"dtype_in": "e4m3 (per-tensor scales amax/448)"} if fp8 else {}),
                            l2="flushed before every timed launch (256 MiB write)",
                            tau=args.tau, exp2_emulation=args.exp2_emulation,
-                           num_splits=args.num_splits, **{"pass": args.pass_}),
+                           num_splits=args.num_splits, precision=args.precision,
+                           **{"pass": args.pass_}),
             "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            **({"pct_of_4500_tflops": 100.0 * value / world / (2 * NOMINAL_BF16_TFLOPS)}
+               if fp8 else {}),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peaks['_source']} bf16_tflops (burst)",
+                         "peak_source": peak_source,
                          "traffic": traffic["bytes"] if traffic else None,
                          "traffic_source": traffic["source"] if traffic else None,
                          "algorithmic_bytes": w_rank.hbm_bytes},
@@ -444,6 +477,8 @@ def main(argv: Optional[List[str]] = None) -> None:
                     help="key-range split forward with this many splits (0: plain forward)")
     ap.add_argument("--exp2-emulation", type=int, choices=[0, 4, 8], default=0,
                     help="one softmax entry pair in N through the software 2^x (0: none)")
+    ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
+                    help="fp8: e4m3 Q, K, V (per-tensor scales) through fa4_fwd_fp8")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
