@@ -55,6 +55,13 @@ class Workload:
         lse = self.B * self.Hq * self.Sq * 4
         return q + kv + o + lse
 
+    @property
+    def hbm_bytes_fp8(self) -> int:
+        """Algorithmic HBM bytes of the FP8 forward: Q, K, V in one byte per
+        element, O in BF16, LSE in fp32."""
+        in_bf16 = (self.B * self.Sq * self.Hq + 2 * self.B * self.Sk * self.Hkv) * self.d * 2
+        return self.hbm_bytes - in_bf16 // 2
+
     def describe(self) -> dict:
         return {
             "workload": self.name, "B": self.B, "Hq": self.Hq, "Hkv": self.Hkv,
