@@ -434,14 +434,14 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   // abort.
   auto issue_pv = [&](int t, int slot, bool first, int phase) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
+    constexpr int kSlices = FP8 ? 1 : FA4_P_SLICES;   // the FP8 P is released whole
 #pragma unroll
-    for (int half = 0; half < FA4_P_SLICES; ++half) {
+    for (int half = 0; half < kSlices; ++half) {
       if (!w.wait_warp(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
       if constexpr (FP8) {
         // 32 keys per step: 8 TMEM columns of packed e4m3 P, 32 rows (4 KB) of V
-        static_assert(FA4_P_SLICES == 1, "the FP8 forward releases P as one block");
         constexpr uint32_t kIdescPv8 = idesc_e4m3_f32(kBM, D, false, true);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
@@ -737,20 +737,17 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       }
     }
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
-    if constexpr (FP8) {
-      tmem_st_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t));
-    }
-    constexpr int kSliceCols = 64 / FA4_P_SLICES;   // TMEM columns of packed P per slice
+    // P goes to the first kPCols columns of S_t, released to the P*V MMAs
+    // in kSlices parts (the FP8 forward always releases it whole)
+    constexpr int kPCols = FP8 ? 32 : 64;
+    constexpr int kSlices = FP8 ? 1 : FA4_P_SLICES;
+    constexpr int kSliceCols = kPCols / kSlices;
 #pragma unroll
-    for (int half = 0; half < (FP8 ? 0 : FA4_P_SLICES); ++half) {
+    for (int half = 0; half < kSlices; ++half) {
 #pragma unroll
       for (int q = 0; q < kSliceCols / 32; ++q)
         tmem_st_x32(s_addr + half * kSliceCols + q * 32,
-                    *reinterpret_cast<const uint32_t(*)[32]>(&pk[(half * kSliceCols + q * 32) % (FP8 ? 32 : 64)]));
+                    *reinterpret_cast<const uint32_t(*)[32]>(&pk[half * kSliceCols + q * 32]));
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
