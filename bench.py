@@ -449,7 +449,8 @@ def run_ours(args, w: workloads.Workload) -> None:
                          "peak_source": peak_source,
                          "traffic": traffic["bytes"] if traffic else None,
                          "traffic_source": traffic["source"] if traffic else None,
-                         "algorithmic_bytes": w_rank.hbm_bytes_fp8 if fp8 else w_rank.hbm_bytes},
+                         "algorithmic_bytes": (w_rank.hbm_bytes_bwd if bwd else
+                                               w_rank.hbm_bytes_fp8 if fp8 else w_rank.hbm_bytes)},
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

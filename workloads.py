@@ -62,6 +62,15 @@ class Workload:
         in_bf16 = (self.B * self.Sq * self.Hq + 2 * self.B * self.Sk * self.Hkv) * self.d * 2
         return self.hbm_bytes - in_bf16 // 2
 
+    @property
+    def hbm_bytes_bwd(self) -> int:
+        """Algorithmic HBM bytes of the backward: Q, K, V, O, dO read and dQ,
+        dK, dV written in BF16, LSE read in fp32."""
+        q = self.B * self.Sq * self.Hq * self.d * 2
+        kv = self.B * self.Sk * self.Hkv * self.d * 2
+        lse = self.B * self.Hq * self.Sq * 4
+        return 3 * q + 2 * kv + lse + q + 2 * kv
+
     def describe(self) -> dict:
         return {
             "workload": self.name, "B": self.B, "Hq": self.Hq, "Hkv": self.Hkv,
