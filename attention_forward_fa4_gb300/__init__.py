@@ -22,7 +22,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["fwd", "fwd_into", "fwd_fp8", "fwd_fp8_into", "exp2_eval", "device_status", "status_string", "version",
+__all__ = ["fwd", "fwd_into", "fwd_host_into", "host_workspace_bytes", "fwd_fp8", "fwd_fp8_into", "exp2_eval", "device_status", "status_string", "version",
            "lib_path", "load_library", "Fa4Error", "FA4_OK", "FA4_ERR_INVALID_ARG",
            "FA4_ERR_UNSUPPORTED", "FA4_ERR_MISALIGNED", "FA4_ERR_CUDA", "FA4_ERR_TIMEOUT"]
 
@@ -76,6 +76,11 @@ def load_library():
     lib.fa4_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                ctypes.POINTER(_Options), vp]
     lib.fa4_fwd_ex.restype = i32
+    lib.fa4_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.fa4_fwd_host_workspace_bytes.restype = ctypes.c_uint64
+    lib.fa4_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp,
+                                 ctypes.c_uint64, vp, vp]
+    lib.fa4_fwd_host.restype = i32
     lib.fa4_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                 f32, f32, f32, vp, vp]
     lib.fa4_fwd_fp8.restype = i32
@@ -280,6 +285,55 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     bwd_into(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, **kw)
     return dq, dk, dv
+
+
+def host_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int) -> int:
+    """Device scratch bytes ``fwd_host_into`` needs."""
+    return int(load_library().fa4_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d))
+
+
+def fwd_host_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                  lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
+                  workspace: torch.Tensor, tau: float = 8.0, exp2_emulation: int = 0,
+                  grid_mode: int = 0, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Forward on HOST tensors (``fa4_fwd_host``): q, k, v, o, lse are CPU
+    tensors (pinned for asynchronous copies) with the layouts of ``fwd_into``;
+    ``workspace`` is a CUDA uint8 tensor of ``host_workspace_bytes(...)``
+    bytes. The copies and the forward are enqueued on ``stream``; o and lse
+    hold the result once the stream has passed the call."""
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,Sq,Hq,d] and k, v [B,Sk,Hkv,d]")
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("o must match q and lse must be [B,Hq,Sq]")
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opt = _Options()
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    opt.tau = float(tau)
+    emu = 8 if exp2_emulation is True else int(exp2_emulation)
+    if emu not in (0, 4, 8):
+        raise ValueError("exp2_emulation must be 0, 4 or 8 (or a bool)")
+    opt.exp2_emulation = emu
+    opt.grid_mode = int(grid_mode)
+    code = lib.fa4_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, Hq, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
+                            workspace.data_ptr(), workspace.numel(), ctypes.byref(opt),
+                            _stream_handle(stream))
+    _check(code, "fa4_fwd_host")
 
 
 def fwd_fp8_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,

@@ -228,7 +228,8 @@ struct Fp8Scales {
 fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                     int Hkv, int Sq, int Sk, int d, float scale, int causal,
                     const fa4_fwd_options* opt, int num_splits, void* workspace,
-                    size_t workspace_bytes, fa4_stream_t stream, const Fp8Scales* fp8 = nullptr) {
+                    size_t workspace_bytes, fa4_stream_t stream, const Fp8Scales* fp8 = nullptr,
+                    bool dry_run = false) {
   using namespace fa4;
   fa4_fwd_options o_def;
   fa4_fwd_default_options(&o_def);
@@ -309,6 +310,7 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if (!status) return FA4_ERR_CUDA;
   const int sms = sm_count(dev);
   if (sms <= 0) return FA4_ERR_CUDA;
+  if (dry_run) return FA4_OK;   // arguments checked, nothing enqueued
   // Grid: one CTA per work tile (the hardware hands the next tile to the
   // first free SM), or persistent (one CTA per SM -- the shared-memory
   // footprint allows no more -- walking its tiles in snake order).
@@ -396,6 +398,56 @@ fa4_status fa4_fwd_fp8(const void* q, const void* k, const void* v, void* o, flo
   const Fp8Scales sc{q_scale, k_scale, v_scale};
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr, 0, stream,
                   &sc);
+}
+
+uint64_t fa4_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || (d != 64 && d != 128)) return 0;
+  auto up = [](uint64_t x) { return (x + 255u) & ~static_cast<uint64_t>(255u); };
+  const uint64_t q = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
+  const uint64_t kv = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
+  const uint64_t lse = static_cast<uint64_t>(B) * Hq * Sq * 4;
+  return 2 * up(q) + 2 * up(kv) + up(lse);
+}
+
+fa4_status fa4_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                        void* workspace, uint64_t workspace_bytes, const fa4_fwd_options* opt,
+                        fa4_stream_t stream) {
+  using namespace fa4;
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return FA4_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
+  const uint64_t need = fa4_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d);
+  if (B == 0 || Sq == 0) return FA4_OK;   // empty output: nothing to copy or compute
+  if (!workspace || workspace_bytes < need) return FA4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA4_ERR_MISALIGNED;
+  if (!q || !o || !lse || (Sk > 0 && (!k || !v))) return FA4_ERR_INVALID_ARG;
+  auto up = [](uint64_t x) { return (x + 255u) & ~static_cast<uint64_t>(255u); };
+  const uint64_t q_bytes = static_cast<uint64_t>(B) * Sq * Hq * d * 2;
+  const uint64_t kv_bytes = static_cast<uint64_t>(B) * Sk * Hkv * d * 2;
+  const uint64_t lse_bytes = static_cast<uint64_t>(B) * Hq * Sq * 4;
+  // workspace: q | k | v | o | lse, each on a 256-byte boundary
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  unsigned char* dq = base;
+  unsigned char* dk = dq + up(q_bytes);
+  unsigned char* dv = dk + up(kv_bytes);
+  unsigned char* dout = dv + up(kv_bytes);
+  float* dlse = reinterpret_cast<float*>(dout + up(q_bytes));
+  fa4_status st = fwd_impl(dq, dk, dv, dout, dlse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0,
+                           nullptr, 0, stream, nullptr, /*dry_run=*/true);
+  if (st != FA4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one copy per tensor, in, the forward, and out, all in stream order
+  if (cudaMemcpyAsync(dq, q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FA4_ERR_CUDA;
+  if (kv_bytes > 0 && (cudaMemcpyAsync(dk, k, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+                       cudaMemcpyAsync(dv, v, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess))
+    return FA4_ERR_CUDA;
+  st = fwd_impl(dq, dk, dv, dout, dlse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr, 0,
+                stream);
+  if (st != FA4_OK) return st;
+  if (cudaMemcpyAsync(o, dout, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FA4_ERR_CUDA;
+  return FA4_OK;
 }
 
 uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_splits) {

@@ -134,6 +134,34 @@ fa4_status fa4_fwd_ex(const void *q, const void *k, const void *v, void *o, floa
                       int causal, const fa4_fwd_options *opt, fa4_stream_t stream);
 
 /*
+ * fa4_fwd_host -- the forward with inputs and outputs in HOST memory: on
+ * `stream`, copies q, k, v into the device workspace (one cudaMemcpyAsync
+ * each), runs the forward there, and copies o and lse back. Meant for
+ * callers whose data lives on the host; host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous. Same operation as
+ * fa4_fwd_ex.
+ *
+ *   q, k, v          HOST, layouts as fa4_fwd (BF16), read
+ *   o, lse           HOST, layouts as fa4_fwd, written once the stream has
+ *                    passed this call (synchronise before reading them)
+ *   workspace        DEVICE scratch owned by the caller, 256-byte aligned, at
+ *                    least fa4_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk,
+ *                    d) bytes: device copies of q, k, v, o and lse in that
+ *                    order, each starting on a 256-byte boundary; it may be
+ *                    reused once the stream has passed this call.
+ *   other arguments as fa4_fwd_ex.
+ * Every argument is checked before anything is enqueued. Returns
+ * FA4_ERR_INVALID_ARG for a missing or small workspace, FA4_ERR_MISALIGNED
+ * for a misaligned one, FA4_ERR_CUDA if a copy cannot be enqueued, and
+ * otherwise as fa4_fwd_ex.
+ */
+uint64_t fa4_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d);
+fa4_status fa4_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale,
+                        int causal, void *workspace, uint64_t workspace_bytes,
+                        const fa4_fwd_options *opt, fa4_stream_t stream);
+
+/*
  * fa4_fwd_fp8 -- the same forward with Q, K and V in FP8 (e4m3): both
  * products run on the tensor cores with 8-bit inputs and an fp32
  * accumulator, the softmax stays in fp32, P is rounded to e4m3 for the
