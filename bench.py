@@ -86,10 +86,10 @@ def kernel_sources_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload_name: str) -> Optional[dict]:
+def stored_traffic(workload_name: str, kernel: str = KERNEL_NAME) -> Optional[dict]:
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload_name}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -466,7 +466,8 @@ def run_ours(args, w: workloads.Workload) -> None:
     peak = float(peaks.get("bf16_tflops", 1900.0)) * (FP8_OVER_BF16 if fp8 else 1.0)
     peak_source = f"{peaks['_source']} bf16_tflops (burst)" + (
         f" x {FP8_OVER_BF16:g} (nominal FP8:BF16 dense ratio)" if fp8 else "")
-    traffic = None if bwd else stored_traffic(w.name + ("_fp8" if fp8 else ""))
+    traffic = (stored_traffic(w.name, "fa4_bwd_kernel") if bwd else
+               stored_traffic(w.name + ("_fp8" if fp8 else "")))
 
     if rank == 0:
         cpu = None

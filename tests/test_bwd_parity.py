@@ -114,3 +114,30 @@ def test_deterministic_mode_repeats_bit_for_bit_and_matches_oracle(case):
     log = [str(case)]
     for name, got in zip(("dq", "dk", "dv"), runs[0]):
         _check(name, got, ref[name], log)
+
+
+@pytest.mark.parametrize("w", [workloads.MID, workloads.LONG_CAUSAL], ids=lambda w: w.name)
+def test_bwd_full_size_sampled_heads(w):
+    """The backward of a full-size workload in the launch the benchmark times
+    (its seeded dO included); the gradients of the first and the last
+    (batch, head) against the fp64 gradient of that head alone, which
+    depends on no other head (Hq = Hkv here)."""
+    fa4 = _fa4()
+    assert w.Hq == w.Hkv
+    q, k, v = workloads.make_inputs(w, seed=0)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa4.fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = fa4.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    code, detail = fa4.device_status(clear=True)
+    assert code == fa4.FA4_OK, f"device status {code} {detail}"
+    for b, h in ((0, 0), (w.B - 1, w.Hq - 1)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ref = ob.attention_bwd(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(),
+                               do[sl].contiguous(), w.scale, w.causal)
+        log = [f"{w.name} b={b} h={h}"]
+        for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+            _check(name, got[sl], ref[name], log)
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dk.float()).all() \
+        and torch.isfinite(dv.float()).all()
