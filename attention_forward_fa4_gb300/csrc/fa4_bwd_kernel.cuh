@@ -79,10 +79,13 @@ struct BwdSmem {
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kQ = 0, kDO = kTileBytes, kLse = 2 * kTileBytes, kDelta = kLse + 512;
   static constexpr int kBars = kStage + kStages * kStageBytes;
-  // barriers: kv, qdo[2], qdo_empty[2], sdp, p_ready, dq_full, dq_free, acc,
-  // stg (the compute warps' rendezvous around the dQ staging tile)
-  static constexpr int bKv = 0, bQdo = 1, bQdoEmpty = 3, bSdp = 5, bPReady = 6, bDqFull = 7,
-                       bDqFree = 8, bAcc = 9, bStgFull = 10, bStgFree = 11, kNumBars = 12;
+  // barriers: kv; per stage Q full / empty and dO (with LSE2, Delta) full /
+  // empty -- dO is released after the dV MMA, Q only after dK, so the next
+  // step's dO arrives first; sdp, p_ready, dq_full, dq_free, acc, stg (the
+  // compute warps' rendezvous around the dQ staging tile)
+  static constexpr int bKv = 0, bQ = 1, bDO = 3, bQEmpty = 5, bDOEmpty = 7, bSdp = 9, bPReady = 10,
+                       bDqFull = 11, bDqFree = 12, bAcc = 13, bStgFull = 14, bStgFree = 15,
+                       kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   // 1 KB of slack re-aligns the base to the 128-byte swizzle's 1 KB period;
@@ -142,34 +145,45 @@ __device__ __forceinline__ void bwd_load_role(const CUtensorMap* tm_q, const CUt
   }
   const int per_head = wk.n_qb - wk.qb0;
   bool ok = true;
-  int s = 0;
-  for (; s < wk.steps; ++s) {
+  int n_do = 0, n_q = 0;        // dO and Q copies issued
+  for (int s = 0; s < wk.steps; ++s) {
     const int h = wk.g * p.group + s / per_head;
     const int qb = wk.qb0 + s % per_head;
     const int st = s % L::kStages;
     const uint32_t stg = sbase + L::stage(s);
-    // the stage's previous step (s - kStages) must be done with it
-    if (s >= L::kStages &&
-        !(ok = w.wait_warp(bar(L::bQdoEmpty + st), static_cast<uint32_t>(s / L::kStages - 1) & 1u,
-                           L::bQdoEmpty + st)))
-      break;
-    mbar_arrive_expect_tx_warp(bar(L::bQdo + st), 2u * L::kTileBytes + 1024u);
+    const uint32_t par = static_cast<uint32_t>(s / L::kStages - 1) & 1u;
+    // dO, LSE2 and Delta of step s, once the stage's previous step
+    // (s - kStages) has finished its dV MMA -- with two stages, its dK MMA
+    // too (both copies then go out together: measured faster at d = 64)
+    const int do_free = L::kStages == 1 ? L::bDOEmpty + st : L::bQEmpty + st;
+    if (s >= L::kStages && !(ok = w.wait_warp(bar(do_free), par, do_free))) break;
+    mbar_arrive_expect_tx_warp(bar(L::bDO + st), L::kTileBytes + 1024u);
 #pragma unroll
-    for (int pn = 0; pn < L::kPanels; ++pn) {
-      tma_load_4d_warp(stg + L::kQ + pn * L::kPanelBytes, tm_q, bar(L::bQdo + st), pn * 64, h, qb * 128, wk.b);
-      tma_load_4d_warp(stg + L::kDO + pn * L::kPanelBytes, tm_do, bar(L::bQdo + st), pn * 64, h, qb * 128,
+    for (int pn = 0; pn < L::kPanels; ++pn)
+      tma_load_4d_warp(stg + L::kDO + pn * L::kPanelBytes, tm_do, bar(L::bDO + st), pn * 64, h, qb * 128,
                        wk.b);
-    }
     const int64_t row0 = (static_cast<int64_t>(wk.b) * p.Hq + h) * p.Sq_pad + qb * 128;
-    bulk_load_warp(stg + L::kLse, p.lse2 + row0, 512u, bar(L::bQdo + st));
-    bulk_load_warp(stg + L::kDelta, p.delta + row0, 512u, bar(L::bQdo + st));
+    bulk_load_warp(stg + L::kLse, p.lse2 + row0, 512u, bar(L::bDO + st));
+    bulk_load_warp(stg + L::kDelta, p.delta + row0, 512u, bar(L::bDO + st));
+    ++n_do;
+    // Q of step s, once that step has finished its dK MMA
+    if (L::kStages == 1 && s >= L::kStages && !(ok = w.wait_warp(bar(L::bQEmpty + st), par, L::bQEmpty + st)))
+      break;
+    mbar_arrive_expect_tx_warp(bar(L::bQ + st), L::kTileBytes);
+#pragma unroll
+    for (int pn = 0; pn < L::kPanels; ++pn)
+      tma_load_4d_warp(stg + L::kQ + pn * L::kPanelBytes, tm_q, bar(L::bQ + st), pn * 64, h, qb * 128, wk.b);
+    ++n_q;
   }
   if (__any_sync(0xffffffffu, !ok || *w.abort)) {
     // Let the copies this warp started land before the CTA exits.
     w.drain_warp(bar(L::bKv), 0u, L::bKv);
-    for (int t = max(0, s - L::kStages); t < s; ++t)
-      w.drain_warp(bar(L::bQdo + t % L::kStages), static_cast<uint32_t>(t / L::kStages) & 1u,
-                   L::bQdo + t % L::kStages);
+    for (int t = max(0, n_do - L::kStages); t < n_do; ++t)
+      w.drain_warp(bar(L::bDO + t % L::kStages), static_cast<uint32_t>(t / L::kStages) & 1u,
+                   L::bDO + t % L::kStages);
+    for (int t = max(0, n_q - L::kStages); t < n_q; ++t)
+      w.drain_warp(bar(L::bQ + t % L::kStages), static_cast<uint32_t>(t / L::kStages) & 1u,
+                   L::bQ + t % L::kStages);
   }
 }
 
@@ -198,22 +212,37 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
     const uint32_t do_lo = desc_lo_sw128(sbase + L::stage(0) + L::kDO, 16) + st * kStageStep;
     const uint32_t q_mn = desc_lo_sw128(sbase + L::stage(0) + L::kQ, L::kPanelBytes) + st * kStageStep;
     const uint32_t do_mn = desc_lo_sw128(sbase + L::stage(0) + L::kDO, L::kPanelBytes) + st * kStageStep;
-    if (!(ok = w.wait_warp(bar(L::bQdo + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bQdo + st)))
-      break;
+    const uint32_t par = static_cast<uint32_t>(s / L::kStages) & 1u;
+    // dP^T = V dO^T into columns that only the previous step's dK MMA
+    // (issued before it) still reads, and S^T = K Q^T (keys on the M side,
+    // queries on N) into columns the previous step's dQ has been read out of.
+    auto issue_dp = [&]() {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+        mma_ss_lohi_warp(tmem + L::kColDP, v_lo + off, kHi, do_lo + off, kHi, kIdescKmaj, kk > 0 ? 1u : 0u);
+      }
+    };
+    if constexpr (L::kStages == 1) {
+      // One Q/dO stage (d = 128): the next step's dO arrives while its Q is
+      // still loading (dO is released after dV, Q after dK), so dP^T goes
+      // first, ahead of the waits for Q and for the dQ read-out. Measured:
+      // +11 % (long causal); with two stages (d = 64) this order lost 3 %.
+      if (!(ok = w.wait_warp(bar(L::bDO + st), par, L::bDO + st))) break;
+      tc_fence_after_sync();
+      issue_dp();
+    }
+    if (!(ok = w.wait_warp(bar(L::bQ + st), par, L::bQ + st))) break;
+    if (L::kStages > 1 && !(ok = w.wait_warp(bar(L::bDO + st), par, L::bDO + st))) break;
     if (s > 0 && !(ok = w.wait_warp(bar(L::bDqFree), static_cast<uint32_t>(s - 1) & 1u, L::bDqFree)))
       break;
     tc_fence_after_sync();
-    // S^T = K Q^T and dP^T = V dO^T (keys on the M side, queries on N)
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
       mma_ss_lohi_warp(tmem + L::kColS, k_lo + off, kHi, q_lo + off, kHi, kIdescKmaj, kk > 0 ? 1u : 0u);
     }
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-      mma_ss_lohi_warp(tmem + L::kColDP, v_lo + off, kHi, do_lo + off, kHi, kIdescKmaj, kk > 0 ? 1u : 0u);
-    }
+    if constexpr (L::kStages > 1) issue_dp();
     mma_commit_warp(bar(L::bSdp));
     if (!(ok = w.wait_warp(bar(L::bPReady), static_cast<uint32_t>(s) & 1u, L::bPReady))) break;
     tc_fence_after_sync();
@@ -224,11 +253,13 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
     for (int kk = 0; kk < 8; ++kk)
       mma_ts_lohi_warp(tmem + L::kColDV, tmem + L::kColS + 32 * (kk >> 1) + 8 * (kk & 1),
                        do_mn + kk * (2048 >> 4), kHi, kIdescTs, (s > 0 || kk > 0) ? 1u : 0u);
+    // dO of this stage read (with two stages the load warp waits for dK)
+    if constexpr (L::kStages == 1) mma_commit_warp(bar(L::bDOEmpty + st));
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ts_lohi_warp(tmem + L::kColDK, tmem + L::kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
                        q_mn + kk * (2048 >> 4), kHi, kIdescTs, (s > 0 || kk > 0) ? 1u : 0u);
-    mma_commit_warp(bar(L::bQdoEmpty + st));
+    mma_commit_warp(bar(L::bQEmpty + st));    // Q of this stage read
     // dQ = dS K over the S^T columns: issued after the dV MMA that reads
     // P^T there (one issuing thread's MMAs execute in order)
 #pragma unroll
@@ -272,7 +303,8 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
     const int st = s % L::kStages;
     const float4* lse4 = reinterpret_cast<const float4*>(smem + L::stage(s) + L::kLse);
     const float4* delta4 = reinterpret_cast<const float4*>(smem + L::stage(s) + L::kDelta);
-    if (!(ok = w.wait(bar(L::bQdo + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bQdo + st)))
+    // LSE2 and Delta arrive with dO
+    if (!(ok = w.wait(bar(L::bDO + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bDO + st)))
       break;
     if (!(ok = w.wait(bar(L::bSdp), static_cast<uint32_t>(s) & 1u, L::bSdp))) break;
     tc_fence_after_sync();
@@ -499,10 +531,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (warp == 1 && lane == 0) {
     mbar_init(bar(L::bKv), 1);
-    mbar_init(bar(L::bQdo), 1);
-    mbar_init(bar(L::bQdo + 1), 1);
-    mbar_init(bar(L::bQdoEmpty), 1);
-    mbar_init(bar(L::bQdoEmpty + 1), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::bQ + i), 1);
+      mbar_init(bar(L::bDO + i), 1);
+      mbar_init(bar(L::bQEmpty + i), 1);
+      mbar_init(bar(L::bDOEmpty + i), 1);
+    }
     mbar_init(bar(L::bSdp), 1);
     mbar_init(bar(L::bPReady), 256);
     mbar_init(bar(L::bDqFull), 1);
