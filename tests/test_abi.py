@@ -106,3 +106,45 @@ def test_trace_layout_matches_header():
     n_st = int(re.search(r"#define FA4_TRACE_STEPS (\d+)", hdr).group(1))
     assert fa4.TRACE_EVENTS == n_ev == len(fa4.TRACE_EVENT_NAMES)
     assert fa4.TRACE_STEPS == n_st
+
+
+def test_fp8_and_host_entry_points_check_arguments_first(lib):
+    """fa4_fwd_fp8 and fa4_fwd_host reject bad arguments before any CUDA
+    call (so the same codes come back with and without a GPU)."""
+    import attention_forward_fa4_gb300 as fa4
+    f32 = ctypes.c_float
+
+    def fp8(d=128, qs=1.0, ks=1.0, vs=1.0, q=Q):
+        return lib.fa4_fwd_fp8(q, K, V, O, L, 1, 2, 2, 64, 64, d, 0.125, 0, f32(qs), f32(ks),
+                               f32(vs), None, None)
+
+    assert fp8(qs=0.0) == fa4.FA4_ERR_INVALID_ARG
+    assert fp8(vs=float("inf")) == fa4.FA4_ERR_INVALID_ARG
+    assert fp8(ks=-1.0) == fa4.FA4_ERR_INVALID_ARG
+    assert fp8(d=64) == fa4.FA4_ERR_UNSUPPORTED
+    assert fp8(q=Q + 8) == fa4.FA4_ERR_MISALIGNED
+    from attention_forward_fa4_gb300 import _Options
+    opt = _Options()
+    lib.fa4_fwd_default_options(ctypes.byref(opt))
+    opt.exp2_emulation = 8
+    assert lib.fa4_fwd_fp8(Q, K, V, O, L, 1, 2, 2, 64, 64, 128, 0.125, 0, f32(1.0), f32(1.0),
+                           f32(1.0), ctypes.byref(opt), None) == fa4.FA4_ERR_UNSUPPORTED
+
+    need = lib.fa4_fwd_host_workspace_bytes(1, 2, 2, 64, 80, 64)
+    # q, o: 16 KB each; k, v: 20 KB each; lse 512 B -> each rounded up to 256 B
+    assert need == 2 * 16384 + 2 * 20480 + 512
+    assert lib.fa4_fwd_host_workspace_bytes(1, 2, 2, 64, 80, 96) == 0
+    W = 8 * P
+
+    def host(ws=W, ws_bytes=need, d=64, B=1, q=Q, scale=0.125):
+        return lib.fa4_fwd_host(q, K, V, O, L, B, 2, 2, 64, 80, d, scale, 0, ws, ws_bytes, None,
+                                None)
+
+    assert host(ws=0) == fa4.FA4_ERR_INVALID_ARG
+    assert host(ws_bytes=need - 1) == fa4.FA4_ERR_INVALID_ARG
+    assert host(ws=W + 128) == fa4.FA4_ERR_MISALIGNED
+    assert host(d=96) == fa4.FA4_ERR_UNSUPPORTED
+    assert host(B=-1) == fa4.FA4_ERR_INVALID_ARG
+    assert host(q=0) == fa4.FA4_ERR_INVALID_ARG
+    assert host(scale=-1.0) == fa4.FA4_ERR_INVALID_ARG
+    assert host(B=0) == fa4.FA4_OK        # empty: nothing to copy or compute
