@@ -467,7 +467,8 @@ def run_ours(args, w: workloads.Workload) -> None:
     peak_source = f"{peaks['_source']} bf16_tflops (burst)" + (
         f" x {FP8_OVER_BF16:g} (nominal FP8:BF16 dense ratio)" if fp8 else "")
     traffic = (stored_traffic(w.name, "fa4_bwd_kernel") if bwd else
-               stored_traffic(w.name + ("_fp8" if fp8 else "")))
+               stored_traffic(w.name + ("_fp8" if fp8 else "")
+                              + (f"_split{args.num_splits}" if args.num_splits else "")))
 
     if rank == 0:
         cpu = None
@@ -535,7 +536,7 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.LONG_CAUSAL.name,
-                    choices=[x.name for x in workloads.ALL_NAMED])
+                    choices=[x.name for x in workloads.ALL_NAMED + workloads.EXTRA])
     ap.add_argument("--tau", type=float, default=8.0)
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward (dQ, dK, dV)")
