@@ -137,7 +137,7 @@ def test_rescale_counter_lazy_below_eager():
 
 # ------------------------------------------------------------ full-size workloads
 FULL = [workloads.TINY, workloads.MID, workloads.LONG_CAUSAL, workloads.GQA_STRESS] + \
-    [w for w in workloads.d64_sweep() if w.Sq in (1024, 32768)]
+    workloads.d64_sweep()
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
