@@ -283,14 +283,22 @@ fa4_status fa4_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
  * allocated or freed at run time). The pages have no counterpart to this
  * entry point; it exists for callers that cannot hand over a workspace.
  *
- * Arguments as fa4_fwd_splitkv without workspace / workspace_bytes. The
- * scratch holds fa4_fwd_splitkv_static_max_bytes() bytes (32 MiB); a call
- * whose fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits) exceeds it
- * returns FA4_ERR_INVALID_ARG with nothing launched.
+ * Arguments as fa4_fwd_splitkv without workspace / workspace_bytes, checked
+ * in the same order and with the same status codes. The scratch holds
+ * fa4_fwd_splitkv_static_max_bytes() bytes (32 MiB); a call with otherwise
+ * valid arguments whose fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d,
+ * num_splits) exceeds it returns FA4_ERR_INVALID_ARG with nothing launched.
+ *
+ * The array lives in the library's module, so it takes its 32 MiB of
+ * device memory on every device where any entry point of this library has
+ * run, whether or not this one is ever called, until the process exits.
  *
  * The first call on each device looks up the scratch's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture. All calls on a device share the one scratch array, so
+ * (cudaGetSymbolAddress) and caches it for the life of the process; make
+ * that first call before any stream capture. The cached address belongs to
+ * the device's primary context: do not use the library on a device after
+ * cudaDeviceReset (or any other teardown of that context) in the same
+ * process. All calls on a device share the one scratch array, so
  * calls whose kernels can overlap in time -- on different streams, or from
  * different host threads without ordering between their streams -- race on
  * it and give undefined results. Calls on one stream are ordered and safe.
