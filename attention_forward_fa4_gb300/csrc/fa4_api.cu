@@ -48,7 +48,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Device address of g_status for the current device (looked up once each).
 // Device address of g_splitkv_scratch for the current device (looked up
 // once each, on the first fa4_fwd_splitkv_static call there).
 void* static_scratch_ptr(int dev) {
@@ -62,6 +61,7 @@ void* static_scratch_ptr(int dev) {
   return addr;
 }
 
+// Device address of g_status for the current device (looked up once each).
 unsigned int* status_ptr(int dev) {
   static std::atomic<unsigned int*> cache[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -76,9 +76,14 @@ unsigned int* status_ptr(int dev) {
 // Automatic grid choice: the persistent grid pays off when work tiles are
 // short (few key blocks each), where per-CTA start-up is a large share of a
 // tile; long tiles keep one CTA per tile and the hardware's dynamic dispatch.
-bool use_persistent_grid(int64_t n_tiles, int sms, int nblk, bool causal) {
-  (void)causal;
-  return n_tiles > sms && nblk <= 8;
+// Measured on GB300 over head dims 64 / 128, 512 to 32768 keys: persistent
+// wins up to 8 key blocks at either head dim, and at head dim 64 up to 16
+// blocks (32 when causal, whose tiles are shorter on average); elsewhere
+// one CTA per tile is as fast or faster.
+bool use_persistent_grid(int64_t n_tiles, int sms, int nblk, int d, bool causal) {
+  if (n_tiles <= sms) return false;
+  if (nblk <= 8) return true;
+  return d == 64 && nblk <= (causal ? 32 : 16);
 }
 
 // Number of SMs of `dev` (looked up once each).
@@ -198,6 +203,7 @@ void fa4_fwd_default_options(fa4_fwd_options* opt) {
   opt->trace_ctas = 0;
   opt->strict_mma_order = 0;
   opt->grid_mode = 0;
+  opt->test_stall_cycles = 0;
 }
 
 const char* fa4_status_string(fa4_status s) {
@@ -246,6 +252,7 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
     return FA4_ERR_INVALID_ARG;
   if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
   if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
+  if (op.test_stall_cycles < 0) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
   if (fp8) {
@@ -314,14 +321,14 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   // Grid: one CTA per work tile (the hardware hands the next tile to the
   // first free SM), or persistent (one CTA per SM -- the shared-memory
   // footprint allows no more -- walking its tiles in snake order).
-  const int nblk = (Sk + 2 * kBM - 1) / kBN;   // key blocks of the longest query tile (upper bound)
+  const int nblk = split_blocks;               // key blocks of the longest work tile
   bool persistent;
   if (op.grid_mode == 1) {
     persistent = false;
   } else if (op.grid_mode == 2) {
     persistent = true;
   } else {
-    persistent = use_persistent_grid(n_tiles, sms, nblk, causal != 0);
+    persistent = use_persistent_grid(n_tiles, sms, nblk, d, causal != 0);
   }
   const int64_t grid = persistent ? (n_tiles < sms ? n_tiles : sms) : n_tiles;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -366,6 +373,7 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.split_blocks = split_blocks;
   p.o_part = o_part;
   p.lse_part = lse_part;
+  p.test_stall_cycles = op.test_stall_cycles;
 
   const int emu = op.exp2_emulation == 1 ? 8 : op.exp2_emulation;   // pair period, 0 = off
   const bool traced = op.trace != nullptr;
@@ -460,7 +468,8 @@ uint64_t fa4_bwd_workspace_bytes(int B, int Hq, int Sq, int d) {
   if (B < 0 || Hq < 0 || Sq < 0 || d < 0) return 0;
   const uint64_t sq_pad = (static_cast<uint64_t>(Sq) + 127) / 128 * 128;
   const uint64_t turns = (static_cast<uint64_t>(B) * Hq * (sq_pad / 128) * 4 + 15) / 16 * 16;
-  return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4 + turns;
+  // + 16 bytes: the deterministic mode's CTA ticket counter
+  return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4 + turns + 16;
 }
 
 fa4_status fa4_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -540,12 +549,14 @@ fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o
   float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
   float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);
   int* turns = reinterpret_cast<int*>(delta + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128));
+  const uint64_t turn_ints = (static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128) * 4 + 15) / 16 * 4;
+  int* ticket = turns + turn_ints;
   cudaError_t err = launch_bwd(tq, tk, tv, tdo, tdq, static_cast<const __nv_bfloat16*>(o),
                                static_cast<const __nv_bfloat16*>(dout), lse,
                                static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta,
-                               deterministic ? turns : nullptr, B, Hq, Hkv, Sq, Sk, d, scale,
-                               causal != 0, status, s);
+                               deterministic ? turns : nullptr, deterministic ? ticket : nullptr,
+                               B, Hq, Hkv, Sq, Sk, d, scale, causal != 0, status, s);
   return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
 }
 
@@ -557,10 +568,15 @@ fa4_status fa4_fwd_splitkv_static(const void* q, const void* k, const void* v, v
                                   fa4_stream_t stream) {
   using namespace fa4;
   if (num_splits < 1 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
+  // Every argument check of the plain forward first (head dim, sizes,
+  // pointers, alignment, device), so the codes match fa4_fwd_splitkv's; the
+  // size cap then rejects only valid problems too large for the scratch.
+  fa4_status st = fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale, causal, opt, 0, nullptr,
+                           0, stream, nullptr, /*dry_run=*/true);
+  if (st != FA4_OK) return st;
+  if (B == 0 || Sq == 0) return FA4_OK;   // empty output: nothing to do
   if (fa4_fwd_splitkv_workspace_bytes(B, Hq, Sq, d, num_splits) > kStaticScratchBytes)
     return FA4_ERR_INVALID_ARG;
-  fa4_status st = check_device();
-  if (st != FA4_OK) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA4_ERR_CUDA;
   void* scratch = static_scratch_ptr(dev);

@@ -66,8 +66,8 @@ cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                         unsigned grid, cudaStream_t s) {
   constexpr int kSmem = BwdSmem<D>::kAlloc;
-  auto kernel = fa4_bwd_kernel<D, CAUSAL>;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kernel = fa4_bwd_kernel<D, CAUSAL>;
+  cudaError_t err = set_smem_once<kernel>(kSmem);
   if (err != cudaSuccess) return err;
   kernel<<<grid, kBwdThreads, kSmem, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
@@ -79,8 +79,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
                        const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
-                       float* dq_acc, float* lse2, float* delta, int* dq_turn, int B, int Hq,
-                       int Hkv, int Sq, int Sk, int d, float scale, bool causal,
+                       float* dq_acc, float* lse2, float* delta, int* dq_turn, int* cta_ticket,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale, bool causal,
                        unsigned int* status, cudaStream_t s) {
   const int Sq_pad = (Sq + 127) / 128 * 128;
   const int64_t dq_elems = static_cast<int64_t>(B) * Sq * Hq * d;
@@ -89,6 +89,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (dq_turn &&
       (err = cudaMemsetAsync(dq_turn, 0, static_cast<size_t>(B) * Hq * (Sq_pad / 128) * 4, s)) != cudaSuccess)
     return err;
+  if (cta_ticket && (err = cudaMemsetAsync(cta_ticket, 0, sizeof(int), s)) != cudaSuccess) return err;
   const int64_t prep_rows = static_cast<int64_t>(B) * Hq * Sq_pad;
   const unsigned prep_blocks = static_cast<unsigned>((prep_rows + 7) / 8);
   if (d == 64)
@@ -115,6 +116,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.dq_turn = dq_turn;
+  p.cta_ticket = cta_ticket;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(p.n_kblk) * B * Hkv);
   if (d == 64)
     err = causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)

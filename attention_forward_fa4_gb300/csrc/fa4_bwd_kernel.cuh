@@ -58,6 +58,10 @@ struct BwdParams {
   // earlier key blocks have added theirs, so the fp32 sums are formed in
   // the same order on every run. CTAs are then numbered key block first.
   int* dq_turn;
+  // Deterministic mode: a zeroed counter from which each CTA takes its work
+  // number when it starts, so every lower number belongs to a CTA that is
+  // already running whatever order the hardware dispatched them in.
+  int* cta_ticket;
 };
 
 // Q, dO, LSE2 and Delta of a step sit in one of kStages stages (two at
@@ -86,7 +90,7 @@ struct BwdSmem {
   static constexpr int bKv = 0, bQ = 1, bDO = 3, bQEmpty = 5, bDOEmpty = 7, bSdp = 9, bPReady = 10,
                        bDqFull = 11, bDqFree = 12, bAcc = 13, bStgFull = 14, bStgFree = 15,
                        kNumBars = 16;
-  static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag
+  static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag, work number
   static constexpr int kBytes = kMisc + 16;
   // 1 KB of slack re-aligns the base to the 128-byte swizzle's 1 KB period;
   // when it does not fit (d = 128) the kernel requires an aligned base.
@@ -104,13 +108,21 @@ struct BwdWork {
   int steps;          // group * (n_qb - qb0)
 };
 
+// The CTA's work number, stored in shared memory by the kernel prologue.
+template <int D>
+__device__ __forceinline__ int bwd_work_id(uint32_t sbase) {
+  int id;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(id) : "r"(sbase + BwdSmem<D>::kMisc + 8) : "memory");
+  return id;
+}
+
 template <bool CAUSAL>
-__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
+__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p, int id) {
   BwdWork w;
-  const int id = static_cast<int>(blockIdx.x);
   // Key blocks of one (batch, kv head) side by side (their CTAs share Q and
-  // dO in L2); in deterministic mode key block first, so every CTA whose
-  // turn comes earlier was dispatched earlier.
+  // dO in L2); in deterministic mode key block first, with work numbers
+  // taken in start order, so every CTA whose turn comes earlier is already
+  // running.
   const int n_bg = p.B * p.Hkv;
   const int kb = p.dq_turn ? id / n_bg : id % p.n_kblk;
   const int bg = p.dq_turn ? id % n_bg : id / p.n_kblk;
@@ -135,7 +147,7 @@ __device__ __forceinline__ void bwd_load_role(const CUtensorMap* tm_q, const CUt
                                               uint32_t sbase, const BwdParams& p, const Waiter& w) {
   using L = BwdSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const BwdWork wk = bwd_work<CAUSAL>(p, bwd_work_id<D>(sbase));
   if (wk.steps == 0) return;
   mbar_arrive_expect_tx_warp(bar(L::bKv), 2u * L::kTileBytes);
 #pragma unroll
@@ -193,7 +205,7 @@ __device__ __forceinline__ void bwd_mma_role(uint32_t sbase, uint32_t tmem, cons
                                              const Waiter& w) {
   using L = BwdSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const BwdWork wk = bwd_work<CAUSAL>(p, bwd_work_id<D>(sbase));
   if (wk.steps == 0) return;
   constexpr uint32_t kIdescKmaj = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t kIdescTs = idesc_bf16_f32(128, D, false, true);        // dV, dK
@@ -290,7 +302,7 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
   const int wq = warp & 3, ch = warp >> 2;             // lane quarter, column half
   const int r = wq * 32 + lane;                         // key row (and dQ query row) = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const BwdWork wk = bwd_work<CAUSAL>(p, bwd_work_id<D>(sbase));
   const int kabs = wk.k0 + r;
   const float c2 = p.scale_log2;
   const int shift = p.Sk - p.Sq;
@@ -447,7 +459,7 @@ __device__ __forceinline__ void bwd_flush_role(const CUtensorMap* tm_dq, uint32_
                                                const BwdParams& p, const Waiter& w) {
   using L = BwdSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_work<CAUSAL>(p);
+  const BwdWork wk = bwd_work<CAUSAL>(p, bwd_work_id<D>(sbase));
   const int per_head = wk.n_qb - wk.qb0;
   const int lane = threadIdx.x & 31;
   const int kb = wk.k0 / 128;
@@ -470,7 +482,7 @@ __device__ __forceinline__ void bwd_flush_role(const CUtensorMap* tm_dq, uint32_
             if (!*w.abort) {
               *w.abort = 1;
               if (atomicCAS(p.status, 0u, kStatusTimeout) == 0u) {
-                p.status[1] = kRoleCorrection;
+                p.status[1] = kRoleFlush;
                 p.status[2] = L::bStgFull;
                 p.status[3] = blockIdx.x;
               }
@@ -530,6 +542,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_relinquish();
   }
   if (warp == 1 && lane == 0) {
+    *reinterpret_cast<volatile int*>(smem + L::kMisc + 8) =
+        p.cta_ticket ? atomicAdd(p.cta_ticket, 1) : static_cast<int>(blockIdx.x);
     mbar_init(bar(L::bKv), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::bQ + i), 1);
@@ -569,7 +583,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const Waiter w{abort_flag, p.status, kRoleMma};
     bwd_mma_role<D, CAUSAL>(sbase, tmem, p, w);
   } else if (warp == kBwdWarpFlush) {
-    const Waiter w{abort_flag, p.status, kRoleCorrection};
+    const Waiter w{abort_flag, p.status, kRoleFlush};
     bwd_flush_role<D, CAUSAL>(&tm_dq, sbase, p, w);
   }
 

@@ -57,6 +57,25 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
+// FA4_WAIT_LANE0  1: the softmax and correction warps poll their barriers
+//                 from lane 0 only and share the outcome with the warp
+//                 (one shared-memory probe per poll instead of 32).
+#ifndef FA4_WAIT_LANE0
+#define FA4_WAIT_LANE0 0
+#endif
+// FA4_K_EARLY      1: the MMA warp waits for K_{j+1} together with V_j, before
+//                  the first P*V of key block j, so nothing separates that
+//                  P*V from the next S MMA.
+#ifndef FA4_K_EARLY
+#define FA4_K_EARLY 0
+#endif
+// FA4_SPEC_EXP     1: after the first key block the softmax exponentiates
+//                  against the current reference max while it forms the
+//                  block max, and redoes the block only when a row of the
+//                  warp moved past tau.
+#ifndef FA4_SPEC_EXP
+#define FA4_SPEC_EXP 0
+#endif
 
 
 namespace fa4 {
@@ -71,7 +90,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimitCycles = 1ll << 30;
 
 enum : unsigned { kStatusTimeout = 5u, kStatusMisalignedSmem = 3u };
-enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3 };
+enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3, kRoleFlush = 4 };
 
 struct FwdParams {
   __nv_bfloat16* o;            // [B, Sq, Hq, D]
@@ -98,6 +117,10 @@ struct FwdParams {
   float* o_part;
   float* lse_part;
   float out_scale;             // multiplies O in the epilogue (V's dequantisation scale; 1 for BF16)
+  // Diagnostic: when > 0 the softmax warps first wait on a barrier that
+  // nothing completes and give up after this many SM cycles, so the kernel
+  // takes its timeout path (abort, drain, free tensor memory, exit).
+  long long test_stall_cycles;
 };
 
 // ------------------------------------------------------------ cycle trace
@@ -178,7 +201,8 @@ struct Smem {
   static constexpr int bQEmpty = bPHalf + 4;             // Q tiles free for the next work tile
   static constexpr int bOFree = bQEmpty + 1;             // [2] epilogue has read O_t
   static constexpr int bDrain = bOFree + 2;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bStall = bDrain + 1;              // never completed (timeout test)
+  static constexpr int kNumBars = bStall + 1;
   // Rescale hand-off from softmax to correction, double-buffered by step
   // parity: alpha float [2 buffers][2 tiles][128], flags int [2][2][4].
   static constexpr int kAlpha = kBars + kNumBars * 8;
@@ -198,7 +222,7 @@ struct Waiter {
   unsigned role;
 
   __device__ __forceinline__ bool slow(uint32_t bar, uint32_t parity, unsigned id,
-                                       bool honour_abort) const {
+                                       bool honour_abort, long long limit = kWaitLimitCycles) const {
     // Poll first; the (cheap, SM-local) cycle counter is only read every
     // 1024 failed polls.
     long long t0 = 0;
@@ -219,7 +243,7 @@ struct Waiter {
         if (honour_abort && *abort) return false;
         const long long now = clock64();
         if (t0 == 0) t0 = now;
-        if (now - t0 > kWaitLimitCycles) {
+        if (now - t0 > limit) {
           *abort = 1;
           if (atomicCAS(status, 0u, kStatusTimeout) == 0u) {
             status[1] = role;
@@ -235,6 +259,25 @@ struct Waiter {
   // Returns false if the CTA is aborting (this wait or another one expired).
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, unsigned id) const {
     return mbar_try_wait(bar, parity) || slow(bar, parity, id, true);
+  }
+  // As wait(), giving up after `limit` SM cycles instead of the default.
+  __device__ __forceinline__ bool wait_for(uint32_t bar, uint32_t parity, unsigned id,
+                                           long long limit) const {
+    return mbar_try_wait(bar, parity) || slow(bar, parity, id, true, limit);
+  }
+  // Per-warp form: lane 0 polls, the warp shares its outcome (and is
+  // synchronised with lane 0 before it returns).
+  __device__ __forceinline__ bool wait_lane0(uint32_t bar, uint32_t parity, unsigned id) const {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = (mbar_try_wait(bar, parity) || slow(bar, parity, id, true)) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+  }
+  // wait() or wait_lane0() by the FA4_WAIT_LANE0 setting.
+  __device__ __forceinline__ bool wait_rows(uint32_t bar, uint32_t parity, unsigned id) const {
+    if (FA4_WAIT_LANE0) return wait_lane0(bar, parity, id);
+    return wait(bar, parity, id);
   }
   // Used only while draining: waits for hardware-driven completions (TMA
   // bytes, MMA commits) even after an abort, still bounded.
@@ -498,6 +541,10 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       if (!(ok = wait_slot(vpos))) break;
       trace_mark_lane0<TRACE>(p, kTrMmaVReady, j, 0, iter);
       bool k_ready = false;
+      if (FA4_K_EARLY && next) {
+        if (!(ok = wait_slot(kpos))) break;
+        k_ready = true;
+      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= tl.nkv[t]) continue;
@@ -573,7 +620,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         if (j >= tl.nkv[t]) continue;
         const int cnt = n_step[t]++;
         const int buf = cnt & 1;
-        if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
+        if (!w.wait_rows(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
         tc_fence_after_sync();
         if (warp == 8 && lane == 0) trace_mark<TRACE>(p, kTrCoWake, j, t, iter);
         const bool flagged = j > 0 && flags_s[(buf * 2 + t) * 4 + wq] != 0;
@@ -585,7 +632,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         if (flagged) {
           // This 32-row group's reference max moved: O_t <- alpha * O_t once
           // the previous P*V into O_t has completed, then release the group.
-          if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
+          if (!w.wait_rows(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
             return;
           tc_fence_after_sync();
 #pragma unroll 1
@@ -622,6 +669,42 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
   }
 }
 
+// One row's 128 exponentials p = 2^(c s + neg_m) on pairs of entries
+// (FFMA2 / FADD2): the row sum of the fp32 p goes to `tot` (two partial
+// halves), P is packed for the P*V MMA (BF16 pairs, or e4m3 quads with
+// FP8). With WITH_MAX the loop also forms the block max of the raw scores
+// in `bmax`.
+template <int EMU_PAIR_PERIOD, bool FP8, bool WITH_MAX>
+__device__ __forceinline__ void exp_pass(const uint32_t (&s)[128], float2 c2, float neg_m,
+                                         uint32_t (&pk)[FP8 ? 32 : 64], float2& tot, float& bmax) {
+  const float2 nm2 = make_float2(neg_m, neg_m);
+  float2 acc[4];
+  float mx[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[i] = make_float2(0.0f, 0.0f);
+    mx[i] = -INFINITY;
+  }
+#pragma unroll
+  for (int pi = 0; pi < 64; ++pi) {
+    const float a = __uint_as_float(s[2 * pi]), b = __uint_as_float(s[2 * pi + 1]);
+    if constexpr (WITH_MAX) mx[pi & 3] = fmax3(mx[pi & 3], a, b);
+    const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
+    const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
+                          ? ex2_emulated2(x)
+                          : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+    acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
+    if constexpr (FP8) {
+      const uint32_t h = pack_e4m3x2(pp.x, pp.y);
+      pk[pi >> 1] = (pi & 1) ? (pk[pi >> 1] | (h << 16)) : h;
+    } else {
+      pk[pi] = pack_bf16x2(pp.x, pp.y);
+    }
+  }
+  tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  if constexpr (WITH_MAX) bmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+}
+
 template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE, bool FP8 = false>
 __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const FwdParams& p, const Waiter& w) {
@@ -641,6 +724,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   int n_step = 0;               // steps of this query tile over all work tiles
   bool ok = true;
   int iter = 0;
+  if (p.test_stall_cycles > 0)   // diagnostic: a wait nothing ends
+    ok = w.wait_for(bar(L::bStall), 0u, L::bStall, p.test_stall_cycles);
   for (int id = tile_of<PERSIST>(0, p.n_tiles); ok && id < p.n_tiles; id = tile_of<PERSIST>(++iter, p.n_tiles)) {
   const Tile tl = make_tile<CAUSAL>(p, id);
   const int row = tl.q0 + t * kBM + r;          // query index
@@ -653,7 +738,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   float l = 0.0f;               // running sum of p relative to m_ref
 
   for (int j = 0; j < n; ++j) {
-    if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
+    if (!(ok = w.wait_rows(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
     tc_fence_after_sync();
     const bool tracer = (wq == 0 && lane == 0);
     if (tracer) trace_mark<TRACE>(p, kTrSmSReady, j, t, iter);
@@ -671,70 +756,88 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
     if (tracer) trace_mark<TRACE>(p, kTrSmLoaded, j, t, iter);
     const int kb = tl.kv0 + j;           // absolute key block
-    if ((kb + 1) * kBN > lim_min) {      // tile-uniform: this block has masked keys
-      const int lim = lim_row - kb * kBN;                // this row's first masked column
+    const bool masked = (kb + 1) * kBN > lim_min;   // tile-uniform: this block has masked keys
+    const int lim = lim_row - kb * kBN;             // this row's first masked column
+    if (masked) {
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : __float_as_uint(-INFINITY);
     }
-    // block max of the raw scores (scale > 0, so max commutes with it)
-    float mx[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-#pragma unroll
-    for (int c = 8; c < 128; c += 8)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-    const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
-    if (tracer) trace_mark<TRACE>(p, kTrSmMaxLoop, j, t, iter);
-    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
-    // than tau, decided per warp so the correction stays warp-uniform.
-    const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-    if (tracer) trace_mark<TRACE>(p, kTrSmCDone, j, t, iter);
-    if (tracer) trace_mark<TRACE>(p, kTrSmMaxDone, j, t, iter);
-    if (warp_need) {
-      const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
-      l *= alpha;
-      if (m_cand != -INFINITY) m_ref = m_cand;
-      alpha_s[(buf * 2 + t) * kBM + r] = alpha;
-      if (j > 0) ++n_rescaled;
-    }
-    if (lane == 0) flags_s[(buf * 2 + t) * 4 + wq] = warp_need ? 1 : 0;
-    // Decision made: the correction warps may read flag / alpha and rescale
-    // O_t while the exponentials run; row groups that need no rescale
-    // release O_t for the next P*V right away. (Every thread arrives on
-    // p_full after its own alpha store; measured faster than one arrival
-    // per warp behind a warp barrier.)
-    mbar_arrive(bar(L::bPFull + t));
-    __syncwarp();
-    if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
-    if (j > 0) ++n_steps;
-    // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
-    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the rest
-    // through MUFU.EX2. The row sum uses the fp32 p; P is stored as BF16.
-    const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
     const float2 c2 = make_float2(cl2, cl2);
-    const float2 nm2 = make_float2(neg_m, neg_m);
-    float2 acc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    float2 tot;
     // P for the P*V MMA: BF16 pairs (64 columns), or with FP8 e4m3 quads
     // (32 columns; key 4i + j in byte j of column i), rounded from fp32
     uint32_t pk[FP8 ? 32 : 64];
-#pragma unroll
-    for (int pi = 0; pi < 64; ++pi) {
-      const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * pi]), __uint_as_float(s[2 * pi + 1])),
-                                  c2, nm2);
-      const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
-                            ? ex2_emulated2(x)
-                            : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-      acc[pi & 3] = __fadd2_rn(acc[pi & 3], pp);
-      if constexpr (FP8) {
-        const uint32_t h = pack_e4m3x2(pp.x, pp.y);
-        pk[pi >> 1] = (pi & 1) ? (pk[pi >> 1] | (h << 16)) : h;
-      } else {
-        pk[pi] = pack_bf16x2(pp.x, pp.y);
+    // Conditional rescale (§3.1.4, Eq. 6): only when the max moved by more
+    // than tau, decided per warp so the correction stays warp-uniform. Once
+    // decided, the correction warps may read flag / alpha and rescale O_t
+    // while the exponentials run; row groups that need no rescale release
+    // O_t for the next P*V right away. (Every thread arrives on p_full after
+    // its own alpha store; measured faster than one arrival per warp behind
+    // a warp barrier.)
+    auto release = [&](float m_cand, bool warp_need) {
+      if (tracer) trace_mark<TRACE>(p, kTrSmCDone, j, t, iter);
+      if (tracer) trace_mark<TRACE>(p, kTrSmMaxDone, j, t, iter);
+      if (warp_need) {
+        const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+        l *= alpha;
+        if (m_cand != -INFINITY) m_ref = m_cand;
+        alpha_s[(buf * 2 + t) * kBM + r] = alpha;
+        if (j > 0) ++n_rescaled;
       }
+      if (lane == 0) flags_s[(buf * 2 + t) * 4 + wq] = warp_need ? 1 : 0;
+      mbar_arrive(bar(L::bPFull + t));
+      __syncwarp();
+      if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
+      if (j > 0) ++n_steps;
+    };
+    // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
+    // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the rest
+    // through MUFU.EX2. The row sum uses the fp32 p; P is stored as BF16.
+    auto neg_ref = [&]() { return (m_ref == -INFINITY) ? 0.0f : -m_ref; };
+    if (FA4_SPEC_EXP && j > 0) {
+      // Speculative pass: exponentiate against the current reference max
+      // while the block max forms in the same loop. Under the lazy rescale
+      // the reference rarely moves; when it does (any row of the warp past
+      // tau), the scores are read again and the block is redone.
+      float bmax;
+      exp_pass<EMU_PAIR_PERIOD, FP8, true>(s, c2, neg_ref(), pk, tot, bmax);
+      const float m_cand = fmaxf(m_ref, bmax * cl2);
+      const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
+      if (!warp_need) {
+        release(m_cand, false);
+      } else {
+        uint32_t s2[128];
+        tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s2[0]));
+        tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s2[32]));
+        tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s2[64]));
+        tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s2[96]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[0]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[32]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[64]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[96]));
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s2[c] = (c < lim) ? s2[c] : __float_as_uint(-INFINITY);
+        }
+        release(m_cand, true);
+        float unused;
+        exp_pass<EMU_PAIR_PERIOD, FP8, false>(s2, c2, neg_ref(), pk, tot, unused);
+      }
+    } else {
+      // block max of the raw scores (scale > 0, so max commutes with it)
+      float mx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+      const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
+      if (tracer) trace_mark<TRACE>(p, kTrSmMaxLoop, j, t, iter);
+      release(m_cand, __any_sync(0xffffffffu, m_cand > m_ref + p.tau));
+      float unused;
+      exp_pass<EMU_PAIR_PERIOD, FP8, false>(s, c2, neg_ref(), pk, tot, unused);
     }
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
     // P goes to the first kPCols columns of S_t, released to the P*V MMAs
@@ -753,7 +856,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t + half));
     }
-    const float2 tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
     l += tot.x + tot.y;
     if (tracer) trace_mark<TRACE>(p, kTrSmArrived, j, t, iter);
     if (lane == 0 && wq > 0) trace_mark<TRACE>(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
@@ -761,7 +863,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // warps must have read it. Checked here, where the warp would otherwise
     // only wait for the next S, rather than on the next step's path.
     if (n_step >= 1 &&
-        !(ok = w.wait(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
+        !(ok = w.wait_rows(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
                       L::bCDone + 2 * t + (buf ^ 1))))
       break;
     ++n_step;
@@ -780,7 +882,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   __nv_bfloat16* orow = p.o + orow_idx * static_cast<int64_t>(D);
   float* prow = p.o_part + (part_off + orow_idx) * static_cast<int64_t>(D);
   if (n > 0) {
-    if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
+    if (!(ok = w.wait_rows(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
       break;
     tc_fence_after_sync();
 #pragma unroll
@@ -873,6 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(L::bQEmpty), 1);
     mbar_init(bar(L::bDrain), 1);
+    mbar_init(bar(L::bStall), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }

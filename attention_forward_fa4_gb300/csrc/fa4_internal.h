@@ -4,9 +4,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fa4_fwd_kernel.cuh"
 
 namespace fa4 {
+
+// Raise KERNEL's dynamic shared-memory limit to `bytes` once per device (the
+// attribute stays set in the device's context; later launches skip the
+// call). One flag bit per device index below 64; others set it every time.
+template <auto KERNEL>
+cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0ull};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit) != 0ull) return cudaSuccess;
+  e = cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Enqueue the forward kernel for head dim 64 / 128. `emu_period` is 0
 // (MUFU.EX2 only), 8 or 4 (one entry pair in 8 / in 4 through the
@@ -30,8 +48,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
                        const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
-                       float* dq_acc, float* lse2, float* delta, int* dq_turn, int B, int Hq,
-                       int Hkv, int Sq, int Sk, int d, float scale, bool causal,
+                       float* dq_acc, float* lse2, float* delta, int* dq_turn, int* cta_ticket,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale, bool causal,
                        unsigned int* status, cudaStream_t s);
 
 // FP8 forward (e4m3 Q, K, V; head dim 128).

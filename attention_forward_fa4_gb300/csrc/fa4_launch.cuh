@@ -11,8 +11,8 @@ template <int D, bool CAUSAL, int EMU, bool PERSIST, bool TRACE, bool FP8 = fals
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, unsigned grid, cudaStream_t stream) {
   constexpr int kSmem = Smem<D, FP8>::kAlloc;
-  auto kernel = fa4_fwd_kernel<D, CAUSAL, EMU, PERSIST, TRACE, FP8>;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kernel = fa4_fwd_kernel<D, CAUSAL, EMU, PERSIST, TRACE, FP8>;
+  cudaError_t err = set_smem_once<kernel>(kSmem);
   if (err != cudaSuccess) return err;
   kernel<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -100,13 +100,21 @@ typedef struct {
      * hardware; 2: persistent, one CTA per SM, each taking work tiles in
      * snake order. Both compute identical results. */
     int grid_mode;
+    /* Diagnostic, 0 by default (must be >= 0). When positive, the softmax
+     * warps of every CTA first wait on a barrier that nothing completes and
+     * give up after this many SM cycles: the kernel then takes its timeout
+     * path (abort flag, in-flight copies and MMAs drained, tensor memory
+     * freed), fa4_device_status reports FA4_ERR_TIMEOUT with role 2
+     * (softmax), and O and LSE are left unwritten. It exercises the abort
+     * path without a GPU fault; the context stays usable. */
+    long long test_stall_cycles;
 } fa4_fwd_options;
 
 #define FA4_TRACE_EVENTS 21
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 0, no counters, no trace,
- * strict_mma_order = 0, grid_mode = 0. */
+ * strict_mma_order = 0, grid_mode = 0, test_stall_cycles = 0. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 
 /*
@@ -208,7 +216,8 @@ fa4_status fa4_fwd_fp8(const void *q, const void *k, const void *v, void *o, flo
  *                    least fa4_bwd_workspace_bytes(B, Hq, Sq, d) bytes: the
  *                    fp32 dQ accumulator [B, Sq, Hq, d], then LSE log2(e)
  *                    and rowsum(dO o O), each [B, Hq, Sq rounded up to 128],
- *                    then one int per (batch, query head, query block).
+ *                    then one int per (batch, query head, query block)
+ *                    (padded to 16 bytes), then one int (the CTA ticket).
  *   other arguments and rules as fa4_fwd; dq, dk, dv and the workspace
  *   must not overlap each other or any input.
  * Enqueues a memset, a preprocessing kernel, the main kernel and a
@@ -225,7 +234,9 @@ fa4_status fa4_bwd(const void *q, const void *k, const void *v, const void *o, c
  * fa4_bwd_ex -- fa4_bwd with deterministic = 0 (the same) or 1: the tiles
  * of dQ that different key blocks contribute are added to the fp32
  * accumulator in key-block order (each CTA waits for its turn on a per
- * query-block counter kept in the workspace), so dq is bit-for-bit the same
+ * query-block counter kept in the workspace; CTAs number their work in the
+ * order they start, from a counter in the workspace, so a CTA only ever
+ * waits for CTAs that are already running), so dq is bit-for-bit the same
  * on every run ("FlashAttention-4: Algorithm and Kernel Pipelining
  * Co-Design for Asymmetric Hardware Scaling", §1: a deterministic execution
  * mode for reproducible training). dk and dv are deterministic in both
@@ -316,8 +327,10 @@ fa4_status fa4_fwd_splitkv_static(const void *q, const void *k, const void *v, v
  * FA4_ERR_MISALIGNED if a backward kernel found its dynamic shared memory
  * not 1 KB aligned (it then exits without work). `detail`
  * (may be NULL) receives 4 words: the error code, the waiting role
- * (0 load, 1 mma, 2 softmax, 3 correction), the barrier id and the block
- * index. When `clear` is non-zero the word is reset to FA4_OK.
+ * (0 load, 1 mma, 2 softmax -- the backward's compute warps --,
+ * 3 correction, 4 the backward's dQ flush warp), the barrier id (an index
+ * into the kernel's own barrier table) and the block index. When `clear`
+ * is non-zero the word is reset to FA4_OK.
  * Returns FA4_ERR_CUDA if the device cannot be reached.
  */
 fa4_status fa4_device_status(int clear, unsigned int *detail);
