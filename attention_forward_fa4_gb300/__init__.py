@@ -48,7 +48,8 @@ class _Options(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("exp2_emulation", ctypes.c_int),
                 ("rescale_stats", ctypes.c_void_p), ("trace", ctypes.c_void_p),
                 ("trace_ctas", ctypes.c_int), ("strict_mma_order", ctypes.c_int),
-                ("grid_mode", ctypes.c_int), ("test_stall_cycles", ctypes.c_longlong)]
+                ("grid_mode", ctypes.c_int), ("correction_warpgroup", ctypes.c_int),
+                ("test_stall_cycles", ctypes.c_longlong)]
 
 
 TRACE_EVENTS = 21
@@ -140,7 +141,8 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              rescale_stats: Optional[torch.Tensor] = None,
              trace: Optional[torch.Tensor] = None, strict_mma_order: bool = False,
              grid_mode: int = 0, num_splits: int = 0,
-             workspace: Optional[torch.Tensor] = None, test_stall_cycles: int = 0,
+             workspace: Optional[torch.Tensor] = None, correction_warpgroup: bool = False,
+             test_stall_cycles: int = 0,
              stream: Optional[torch.cuda.Stream] = None) -> None:
     """Write attention forward into preallocated ``o`` and ``lse``.
 
@@ -179,6 +181,7 @@ def fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     opt.strict_mma_order = 1 if strict_mma_order else 0
     opt.grid_mode = int(grid_mode)
     opt.test_stall_cycles = int(test_stall_cycles)
+    opt.correction_warpgroup = 1 if correction_warpgroup else 0
     if rescale_stats is not None:
         if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
             raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")
@@ -342,6 +345,7 @@ def fwd_fp8_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Ten
                  causal: bool = False, scale: Optional[float] = None, *, tau: float = 8.0,
                  rescale_stats: Optional[torch.Tensor] = None,
                  strict_mma_order: bool = False, grid_mode: int = 0,
+                 correction_warpgroup: bool = False,
                  stream: Optional[torch.cuda.Stream] = None) -> None:
     """FP8 forward (``fa4_fwd_fp8``) into preallocated ``o`` and ``lse``.
 
@@ -375,6 +379,7 @@ def fwd_fp8_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Ten
     opt.tau = float(tau)
     opt.strict_mma_order = 1 if strict_mma_order else 0
     opt.grid_mode = int(grid_mode)
+    opt.correction_warpgroup = 1 if correction_warpgroup else 0
     if rescale_stats is not None:
         if rescale_stats.dtype != torch.int64 or rescale_stats.numel() < 2 or not rescale_stats.is_cuda:
             raise ValueError("rescale_stats must be a CUDA int64 tensor of 2 elements")

@@ -203,6 +203,7 @@ void fa4_fwd_default_options(fa4_fwd_options* opt) {
   opt->trace_ctas = 0;
   opt->strict_mma_order = 0;
   opt->grid_mode = 0;
+  opt->correction_warpgroup = 0;
   opt->test_stall_cycles = 0;
 }
 
@@ -253,6 +254,7 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if (op.strict_mma_order != 0 && op.strict_mma_order != 1) return FA4_ERR_INVALID_ARG;
   if (op.grid_mode < 0 || op.grid_mode > 2) return FA4_ERR_INVALID_ARG;
   if (op.test_stall_cycles < 0) return FA4_ERR_INVALID_ARG;
+  if (op.correction_warpgroup != 0 && op.correction_warpgroup != 1) return FA4_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA4_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > kMaxSplits) return FA4_ERR_INVALID_ARG;
   if (fp8) {
@@ -374,6 +376,7 @@ fa4_status fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.o_part = o_part;
   p.lse_part = lse_part;
   p.test_stall_cycles = op.test_stall_cycles;
+  p.correction_wg = op.correction_warpgroup;
 
   const int emu = op.exp2_emulation == 1 ? 8 : op.exp2_emulation;   // pair period, 0 = off
   const bool traced = op.trace != nullptr;

@@ -11,3 +11,13 @@ cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
 }
 
 }  // namespace fa4
+
+#ifdef FA4_PROF
+// Diagnostic builds: read and clear the phase profile of the head-dim-128
+// kernels (32 uint64 sums).
+extern "C" int fa4_prof_read_d128(unsigned long long* out) {
+  if (cudaMemcpyFromSymbol(out, fa4::g_prof, sizeof(unsigned long long) * 32) != cudaSuccess) return 1;
+  const unsigned long long z[32] = {};
+  return cudaMemcpyToSymbol(fa4::g_prof, z, sizeof z) != cudaSuccess;
+}
+#endif

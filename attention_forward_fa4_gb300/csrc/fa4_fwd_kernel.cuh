@@ -57,28 +57,20 @@
 #ifndef FA4_WAIT_SPIN
 #define FA4_WAIT_SPIN 0
 #endif
-// FA4_WAIT_LANE0  1: the softmax and correction warps poll their barriers
-//                 from lane 0 only and share the outcome with the warp
-//                 (one shared-memory probe per poll instead of 32).
-#ifndef FA4_WAIT_LANE0
-#define FA4_WAIT_LANE0 0
-#endif
-// FA4_K_EARLY      1: the MMA warp waits for K_{j+1} together with V_j, before
-//                  the first P*V of key block j, so nothing separates that
-//                  P*V from the next S MMA.
-#ifndef FA4_K_EARLY
-#define FA4_K_EARLY 0
-#endif
-// FA4_SPEC_EXP     1: after the first key block the softmax exponentiates
-//                  against the current reference max while it forms the
-//                  block max, and redoes the block only when a row of the
-//                  warp moved past tau.
-#ifndef FA4_SPEC_EXP
-#define FA4_SPEC_EXP 0
-#endif
 
 
 namespace fa4 {
+
+#ifdef FA4_PROF
+// Light phase profile (diagnostic builds only): cycle sums added once per
+// role at exit. [0..5] softmax of the tile-0 warp 0: load, decide, exp,
+// store, wait for S, steps; [8..13] MMA warp: wait for the softmax,
+// P*V issue, between P*V and S, S issue, steps.
+__device__ unsigned long long g_prof[32];
+#define FA4_PROF_CLK(x) const unsigned x = static_cast<unsigned>(clock())
+#else
+#define FA4_PROF_CLK(x)
+#endif
 
 constexpr int kBM = 128;          // query rows per tile = TMEM lanes
 constexpr int kBN = 128;          // keys per block
@@ -117,6 +109,9 @@ struct FwdParams {
   float* o_part;
   float* lse_part;
   float out_scale;             // multiplies O in the epilogue (V's dequantisation scale; 1 for BF16)
+  // 1: a correction warpgroup rescales O_t when a row group's reference max
+  // moves; 0: the softmax warp of that row group does it itself.
+  int correction_wg;
   // Diagnostic: when > 0 the softmax warps first wait on a barrier that
   // nothing completes and give up after this many SM cycles, so the kernel
   // takes its timeout path (abort, drain, free tensor memory, exit).
@@ -264,20 +259,6 @@ struct Waiter {
   __device__ __forceinline__ bool wait_for(uint32_t bar, uint32_t parity, unsigned id,
                                            long long limit) const {
     return mbar_try_wait(bar, parity) || slow(bar, parity, id, true, limit);
-  }
-  // Per-warp form: lane 0 polls, the warp shares its outcome (and is
-  // synchronised with lane 0 before it returns).
-  __device__ __forceinline__ bool wait_lane0(uint32_t bar, uint32_t parity, unsigned id) const {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = (mbar_try_wait(bar, parity) || slow(bar, parity, id, true)) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-  }
-  // wait() or wait_lane0() by the FA4_WAIT_LANE0 setting.
-  __device__ __forceinline__ bool wait_rows(uint32_t bar, uint32_t parity, unsigned id) const {
-    if (FA4_WAIT_LANE0) return wait_lane0(bar, parity, id);
-    return wait(bar, parity, id);
   }
   // Used only while draining: waits for hardware-driven completions (TMA
   // bytes, MMA commits) even after an abort, still bounded.
@@ -445,6 +426,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   constexpr uint32_t kHi = desc_hi_sw128(1024);                          // 8 rows x 128 B
   const uint32_t col_s[2] = {L::kColS0, L::kColS1};
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+#ifdef FA4_PROF
+  unsigned pm_acc[4] = {0, 0, 0, 0}, pm_n = 0, pm_pw = 0;
+#endif
   // Low descriptor halves: K-major operands (LBO unused = 16 B), V with the
   // 64-column panel stride as LBO.
   const uint32_t q_lo[2] = {desc_lo_sw128(sbase + L::kQ, 16),
@@ -483,6 +467,9 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       if (!w.wait_warp(bar(L::bPHalf + 2 * t + half), static_cast<uint32_t>(phase) & 1u, L::bPHalf + 2 * t + half))
         return false;
       tc_fence_after_sync();
+#ifdef FA4_PROF
+      pm_pw = static_cast<unsigned>(clock());
+#endif
       if constexpr (FP8) {
         // 32 keys per step: 8 TMEM columns of packed e4m3 P, 32 rows (4 KB) of V
         constexpr uint32_t kIdescPv8 = idesc_e4m3_f32(kBM, D, false, true);
@@ -541,14 +528,11 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
       if (!(ok = wait_slot(vpos))) break;
       trace_mark_lane0<TRACE>(p, kTrMmaVReady, j, 0, iter);
       bool k_ready = false;
-      if (FA4_K_EARLY && next) {
-        if (!(ok = wait_slot(kpos))) break;
-        k_ready = true;
-      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= tl.nkv[t]) continue;
         trace_mark_lane0<TRACE>(p, kTrMmaPvWait, j, t, iter);
+        FA4_PROF_CLK(pm_a);
         if (!(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
           break;
         if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
@@ -558,6 +542,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
         trace_mark_lane0<TRACE>(p, kTrMmaPvGo, j, t, iter);
         if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t]))) break;
         ++n_pv[t];
+        FA4_PROF_CLK(pm_b);
         trace_mark_lane0<TRACE>(p, kTrMmaPvIssued, j, t, iter);
         if (j + 1 >= tl.nkv[t]) continue;
         trace_mark_lane0<TRACE>(p, kTrMmaSWait, j + 1, t, iter);
@@ -572,7 +557,18 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
           tc_fence_after_sync();
         }
         trace_mark_lane0<TRACE>(p, kTrMmaSGo, j + 1, t, iter);
+        FA4_PROF_CLK(pm_c);
         issue_s(t, kpos % L::kSlots);
+#ifdef FA4_PROF
+        if (j > 0) {
+          const unsigned pm_d = static_cast<unsigned>(clock());
+          pm_acc[0] += pm_pw - pm_a;
+          pm_acc[1] += pm_b - pm_pw;
+          pm_acc[2] += pm_c - pm_b;
+          pm_acc[3] += pm_d - pm_c;
+          ++pm_n;
+        }
+#endif
         trace_mark_lane0<TRACE>(p, kTrMmaSIssued, j + 1, t, iter);
       }
       if (!ok) break;
@@ -595,6 +591,12 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   // Every MMA issued above has completed once this commit arrives.
   mma_commit_warp(bar(L::bDrain));
   w.drain_warp(bar(L::bDrain), 0u, L::bDrain);
+#ifdef FA4_PROF
+  if ((threadIdx.x & 31) == 0) {
+    for (int i = 0; i < 4; ++i) atomicAdd(&g_prof[8 + i], static_cast<unsigned long long>(pm_acc[i]));
+    atomicAdd(&g_prof[12], static_cast<unsigned long long>(pm_n));
+  }
+#endif
 }
 
 // ------------------------------------------------------------ correction WG
@@ -607,7 +609,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
   const int wq = warp & 3;
   const int r = wq * 32 + lane;
   const float* alpha_s = reinterpret_cast<const float*>(smem + L::kAlpha);
-  const volatile int* flags_s = reinterpret_cast<const volatile int*>(smem + L::kFlags);
+  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + L::kFlags);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
   int n_step[2] = {0, 0};       // softmax steps seen per query tile (all work tiles)
@@ -620,10 +622,14 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         if (j >= tl.nkv[t]) continue;
         const int cnt = n_step[t]++;
         const int buf = cnt & 1;
-        if (!w.wait_rows(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
+        if (!w.wait(bar(L::bPFull + t), static_cast<uint32_t>(cnt) & 1u, L::bPFull + t)) return;
         tc_fence_after_sync();
         if (warp == 8 && lane == 0) trace_mark<TRACE>(p, kTrCoWake, j, t, iter);
-        const bool flagged = j > 0 && flags_s[(buf * 2 + t) * 4 + wq] != 0;
+        const int fval = flags_s[(buf * 2 + t) * 4 + wq];
+        const bool flagged = j > 0 && fval != 0;
+        // a set flag is cleared here, so a step that needs no rescale
+        // stores nothing before its p_full arrival
+        if (fval != 0 && lane == 0) flags_s[(buf * 2 + t) * 4 + wq] = 0;
         const float a = flagged ? alpha_s[(buf * 2 + t) * kBM + r] : 1.0f;
         // this buffer's flags and alpha are read: the softmax may reuse it
         // two steps on
@@ -632,7 +638,7 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         if (flagged) {
           // This 32-row group's reference max moved: O_t <- alpha * O_t once
           // the previous P*V into O_t has completed, then release the group.
-          if (!w.wait_rows(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
+          if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
             return;
           tc_fence_after_sync();
 #pragma unroll 1
@@ -672,24 +678,18 @@ __host__ __device__ constexpr bool emulated_pair(int pi) {
 // One row's 128 exponentials p = 2^(c s + neg_m) on pairs of entries
 // (FFMA2 / FADD2): the row sum of the fp32 p goes to `tot` (two partial
 // halves), P is packed for the P*V MMA (BF16 pairs, or e4m3 quads with
-// FP8). With WITH_MAX the loop also forms the block max of the raw scores
-// in `bmax`.
-template <int EMU_PAIR_PERIOD, bool FP8, bool WITH_MAX>
+// FP8).
+template <int EMU_PAIR_PERIOD, bool FP8>
 __device__ __forceinline__ void exp_pass(const uint32_t (&s)[128], float2 c2, float neg_m,
-                                         uint32_t (&pk)[FP8 ? 32 : 64], float2& tot, float& bmax) {
+                                         uint32_t (&pk)[FP8 ? 32 : 64], float2& tot) {
   const float2 nm2 = make_float2(neg_m, neg_m);
   float2 acc[4];
-  float mx[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc[i] = make_float2(0.0f, 0.0f);
-    mx[i] = -INFINITY;
-  }
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int pi = 0; pi < 64; ++pi) {
-    const float a = __uint_as_float(s[2 * pi]), b = __uint_as_float(s[2 * pi + 1]);
-    if constexpr (WITH_MAX) mx[pi & 3] = fmax3(mx[pi & 3], a, b);
-    const float2 x = __ffma2_rn(make_float2(a, b), c2, nm2);
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * pi]), __uint_as_float(s[2 * pi + 1])),
+                                c2, nm2);
     const float2 pp = emulated_pair<EMU_PAIR_PERIOD>(pi)
                           ? ex2_emulated2(x)
                           : make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
@@ -702,7 +702,6 @@ __device__ __forceinline__ void exp_pass(const uint32_t (&s)[128], float2 c2, fl
     }
   }
   tot = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-  if constexpr (WITH_MAX) bmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
 }
 
 template <int D, bool CAUSAL, int EMU_PAIR_PERIOD, bool PERSIST, bool TRACE, bool FP8 = false>
@@ -721,6 +720,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   const float cl2 = p.scale_log2;
   const int shift = p.Sk - p.Sq;
   unsigned n_rescaled = 0, n_steps = 0;
+#ifdef FA4_PROF
+  unsigned pr_acc[5] = {0, 0, 0, 0, 0}, pr_prev_arrived = 0, pr_n = 0;
+#endif
   int n_step = 0;               // steps of this query tile over all work tiles
   bool ok = true;
   int iter = 0;
@@ -738,8 +740,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   float l = 0.0f;               // running sum of p relative to m_ref
 
   for (int j = 0; j < n; ++j) {
-    if (!(ok = w.wait_rows(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
+    if (!(ok = w.wait(bar(L::bSFull + t), static_cast<uint32_t>(n_step) & 1u, L::bSFull + t))) break;
     tc_fence_after_sync();
+    FA4_PROF_CLK(pr_t0);
     const bool tracer = (wq == 0 && lane == 0);
     if (tracer) trace_mark<TRACE>(p, kTrSmSReady, j, t, iter);
     uint32_t s[128];
@@ -754,6 +757,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    FA4_PROF_CLK(pr_t1);
     if (tracer) trace_mark<TRACE>(p, kTrSmLoaded, j, t, iter);
     const int kb = tl.kv0 + j;           // absolute key block
     const bool masked = (kb + 1) * kBN > lim_min;   // tile-uniform: this block has masked keys
@@ -774,9 +778,48 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // O_t for the next P*V right away. (Every thread arrives on p_full after
     // its own alpha store; measured faster than one arrival per warp behind
     // a warp barrier.)
+#ifdef FA4_PROF
+    unsigned pr_t2 = 0;
+#endif
+    bool inline_ok = true;
     auto release = [&](float m_cand, bool warp_need) {
       if (tracer) trace_mark<TRACE>(p, kTrSmCDone, j, t, iter);
       if (tracer) trace_mark<TRACE>(p, kTrSmMaxDone, j, t, iter);
+      if (!p.correction_wg) {
+        if (warp_need) {
+          const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
+          l *= alpha;
+          if (m_cand != -INFINITY) m_ref = m_cand;
+          if (j > 0) {
+            ++n_rescaled;
+            // O_t <- alpha * O_t for this warp's rows, once the previous P*V
+            // into O_t has completed
+            if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)) {
+              inline_ok = false;
+              return;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t x[16];
+              tmem_ld_x16(o_addr + c * 16, x);
+              tmem_wait_ld_x16(x);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
+              tmem_st_x16(o_addr + c * 16, x);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bOReady + t));
+        if (j > 0) ++n_steps;
+#ifdef FA4_PROF
+        pr_t2 = static_cast<unsigned>(clock());
+#endif
+        return;
+      }
       if (warp_need) {
         const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
         l *= alpha;
@@ -784,46 +827,20 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
         alpha_s[(buf * 2 + t) * kBM + r] = alpha;
         if (j > 0) ++n_rescaled;
       }
-      if (lane == 0) flags_s[(buf * 2 + t) * 4 + wq] = warp_need ? 1 : 0;
+      if (lane == 0 && warp_need) flags_s[(buf * 2 + t) * 4 + wq] = 1;
       mbar_arrive(bar(L::bPFull + t));
       __syncwarp();
       if (lane == 0 && (!warp_need || j == 0)) mbar_arrive(bar(L::bOReady + t));
       if (j > 0) ++n_steps;
+#ifdef FA4_PROF
+      pr_t2 = static_cast<unsigned>(clock());
+#endif
     };
     // p = 2^(c*s - m_ref) on pairs of entries (FFMA2 / FADD2); one pair in
     // EMU_PAIR_PERIOD goes through the FMA-pipe emulation (§3.1.3), the rest
     // through MUFU.EX2. The row sum uses the fp32 p; P is stored as BF16.
     auto neg_ref = [&]() { return (m_ref == -INFINITY) ? 0.0f : -m_ref; };
-    if (FA4_SPEC_EXP && j > 0) {
-      // Speculative pass: exponentiate against the current reference max
-      // while the block max forms in the same loop. Under the lazy rescale
-      // the reference rarely moves; when it does (any row of the warp past
-      // tau), the scores are read again and the block is redone.
-      float bmax;
-      exp_pass<EMU_PAIR_PERIOD, FP8, true>(s, c2, neg_ref(), pk, tot, bmax);
-      const float m_cand = fmaxf(m_ref, bmax * cl2);
-      const bool warp_need = __any_sync(0xffffffffu, m_cand > m_ref + p.tau);
-      if (!warp_need) {
-        release(m_cand, false);
-      } else {
-        uint32_t s2[128];
-        tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s2[0]));
-        tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s2[32]));
-        tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s2[64]));
-        tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s2[96]));
-        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[0]));
-        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[32]));
-        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[64]));
-        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s2[96]));
-        if (masked) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s2[c] = (c < lim) ? s2[c] : __float_as_uint(-INFINITY);
-        }
-        release(m_cand, true);
-        float unused;
-        exp_pass<EMU_PAIR_PERIOD, FP8, false>(s2, c2, neg_ref(), pk, tot, unused);
-      }
-    } else {
+    {
       // block max of the raw scores (scale > 0, so max commutes with it)
       float mx[4];
 #pragma unroll
@@ -836,9 +853,10 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       const float m_cand = fmaxf(m_ref, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * cl2);
       if (tracer) trace_mark<TRACE>(p, kTrSmMaxLoop, j, t, iter);
       release(m_cand, __any_sync(0xffffffffu, m_cand > m_ref + p.tau));
-      float unused;
-      exp_pass<EMU_PAIR_PERIOD, FP8, false>(s, c2, neg_ref(), pk, tot, unused);
+      exp_pass<EMU_PAIR_PERIOD, FP8>(s, c2, neg_ref(), pk, tot);
     }
+    if (!(ok = inline_ok)) break;
+    FA4_PROF_CLK(pr_t3);
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
     // P goes to the first kPCols columns of S_t, released to the P*V MMAs
     // in kSlices parts (the FP8 forward always releases it whole)
@@ -857,13 +875,27 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       if (lane == 0) mbar_arrive(bar(L::bPHalf + 2 * t + half));
     }
     l += tot.x + tot.y;
+#ifdef FA4_PROF
+    {
+      const unsigned pr_t4 = static_cast<unsigned>(clock());
+      if (j > 0) {
+        pr_acc[0] += pr_t1 - pr_t0;
+        pr_acc[1] += pr_t2 - pr_t1;
+        pr_acc[2] += pr_t3 - pr_t2;
+        pr_acc[3] += pr_t4 - pr_t3;
+        pr_acc[4] += pr_t0 - pr_prev_arrived;
+        ++pr_n;
+      }
+      pr_prev_arrived = pr_t4;
+    }
+#endif
     if (tracer) trace_mark<TRACE>(p, kTrSmArrived, j, t, iter);
     if (lane == 0 && wq > 0) trace_mark<TRACE>(p, kTrSmArrivedQ1 + wq - 1, j, t, iter);
     // The next step reuses the buffer of step n_step - 1: the correction
     // warps must have read it. Checked here, where the warp would otherwise
     // only wait for the next S, rather than on the next step's path.
-    if (n_step >= 1 &&
-        !(ok = w.wait_rows(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
+    if (p.correction_wg && n_step >= 1 &&
+        !(ok = w.wait(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
                       L::bCDone + 2 * t + (buf ^ 1))))
       break;
     ++n_step;
@@ -882,7 +914,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   __nv_bfloat16* orow = p.o + orow_idx * static_cast<int64_t>(D);
   float* prow = p.o_part + (part_off + orow_idx) * static_cast<int64_t>(D);
   if (n > 0) {
-    if (!(ok = w.wait_rows(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
+    if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
       break;
     tc_fence_after_sync();
 #pragma unroll
@@ -935,6 +967,12 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     atomicAdd(&p.stats[0], static_cast<unsigned long long>(n_rescaled));
     atomicAdd(&p.stats[1], static_cast<unsigned long long>(n_steps));
   }
+#ifdef FA4_PROF
+  if (t == 0 && wq == 0 && lane == 0) {
+    for (int i = 0; i < 5; ++i) atomicAdd(&g_prof[i], static_cast<unsigned long long>(pr_acc[i]));
+    atomicAdd(&g_prof[5], static_cast<unsigned long long>(pr_n));
+  }
+#endif
 }
 
 // ------------------------------------------------------------ kernel
@@ -976,6 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::bQEmpty), 1);
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bStall), 1);
+    for (int i = 0; i < 16; ++i) reinterpret_cast<volatile int*>(smem + L::kFlags)[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1003,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     regs_decrease<kRegsCorrection>();
     const Waiter w{abort_flag, p.status, kRoleCorrection};
-    correction_role<D, CAUSAL, PERSIST, TRACE, FP8>(sbase, smem, tmem, p, w);
+    if (p.correction_wg) correction_role<D, CAUSAL, PERSIST, TRACE, FP8>(sbase, smem, tmem, p, w);
   } else {
     regs_decrease<kRegsLoadMma>();
     if (warp == kWarpLoad) {

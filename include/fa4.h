@@ -100,6 +100,15 @@ typedef struct {
      * hardware; 2: persistent, one CTA per SM, each taking work tiles in
      * snake order. Both compute identical results. */
     int grid_mode;
+    /* Who rescales the output accumulator when a row group's reference
+     * maximum moves (the conditional rescale of "FlashAttention-4" §3.1.4):
+     * 0 (default): the softmax warp of those 32 rows, before it releases
+     * the accumulator to the next P*V -- under tau = 8 rescales are rare
+     * (on the GQA stress workload 0.3 % of row-group steps), and on GB300
+     * dropping the per-step hand-off measured 2-10 % faster; 1: a separate
+     * correction warpgroup, off the softmax's path, as the pages describe
+     * (§3.1.2). Both compute identical results. */
+    int correction_warpgroup;
     /* Diagnostic, 0 by default (must be >= 0). When positive, the softmax
      * warps of every CTA first wait on a barrier that nothing completes and
      * give up after this many SM cycles: the kernel then takes its timeout
@@ -114,7 +123,8 @@ typedef struct {
 #define FA4_TRACE_STEPS 128
 
 /* Default options: tau = 8, exp2_emulation = 0, no counters, no trace,
- * strict_mma_order = 0, grid_mode = 0, test_stall_cycles = 0. */
+ * strict_mma_order = 0, grid_mode = 0, correction_warpgroup = 0,
+ * test_stall_cycles = 0. */
 void fa4_fwd_default_options(fa4_fwd_options *opt);
 
 /*

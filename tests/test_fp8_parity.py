@@ -68,18 +68,21 @@ def test_small_shapes_match_oracle(case, grid_mode):
     _full_check(inputs, causal, 1.0 / math.sqrt(128), str(case), grid_mode=grid_mode)
 
 
-def test_large_logits_match_oracle():
+@pytest.mark.parametrize("cwg", [False, True], ids=["inline", "corr_wg"])
+def test_large_logits_match_oracle(cwg):
     # |scores| ~ 16 x larger: row maxima jump between blocks, rescales fire.
     inputs = workloads.make_custom_fp8(2, 2, 2, 384, 640, 128, seed=52, dist="wide")
     for causal in (False, True):
-        _full_check(inputs, causal, 1 / math.sqrt(128), f"wide causal={causal}")
+        _full_check(inputs, causal, 1 / math.sqrt(128), f"wide causal={causal}",
+                    correction_warpgroup=cwg)
 
 
+@pytest.mark.parametrize("cwg", [False, True], ids=["inline", "corr_wg"])
 @pytest.mark.parametrize("tau", [0.0, 8.0])
-def test_eager_and_lazy_rescale_both_match(tau):
+def test_eager_and_lazy_rescale_both_match(tau, cwg):
     w = workloads.Workload("ramp", 1, 4, 1, 1024, 1024, 128, True, ramp=0.03)
     inputs = workloads.make_inputs_fp8(w, seed=0)
-    _full_check(inputs, True, w.scale, f"tau={tau}", tau=tau)
+    _full_check(inputs, True, w.scale, f"tau={tau}", tau=tau, correction_warpgroup=cwg)
 
 
 def test_scales_enter_as_the_definition_says():

@@ -67,18 +67,41 @@ def test_small_shapes_match_oracle(case, emu):
     _full_check(q, k, v, causal, 1.0 / math.sqrt(d), str(case), exp2_emulation=emu)
 
 
-def test_large_logits_match_oracle():
+@pytest.mark.parametrize("cwg", [False, True], ids=["inline", "corr_wg"])
+def test_large_logits_match_oracle(cwg):
     # |scores| ~ 16 x larger: row maxima jump between blocks, rescales fire.
     q, k, v = workloads.make_custom(2, 2, 2, 384, 640, 128, seed=32, dist="wide")
     for causal in (False, True):
-        _full_check(q, k, v, causal, 1 / math.sqrt(128), f"wide causal={causal}")
+        _full_check(q, k, v, causal, 1 / math.sqrt(128), f"wide causal={causal}",
+                    correction_warpgroup=cwg)
 
 
+@pytest.mark.parametrize("cwg", [False, True], ids=["inline", "corr_wg"])
 @pytest.mark.parametrize("tau", [0.0, 8.0])
-def test_eager_and_lazy_rescale_both_match(tau):
+def test_eager_and_lazy_rescale_both_match(tau, cwg):
     w = workloads.Workload("ramp", 1, 4, 1, 1024, 1024, 128, True, ramp=0.03)
     q, k, v = workloads.make_inputs(w, seed=0)
-    _full_check(q, k, v, True, w.scale, f"tau={tau}", tau=tau)
+    _full_check(q, k, v, True, w.scale, f"tau={tau}", tau=tau, correction_warpgroup=cwg)
+
+
+@pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_small_shapes_with_correction_warpgroup(case):
+    B, Hq, Hkv, Sq, Sk, d, causal = case
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=31, dist="wide")
+    _full_check(q, k, v, causal, 1.0 / math.sqrt(d), str(case), correction_warpgroup=True)
+
+
+@pytest.mark.parametrize("shape", [(2, 4, 4, 1100, 1300, 128, True), (1, 8, 2, 900, 2100, 64, False),
+                                   (2, 4, 2, 700, 700, 64, True)])
+@pytest.mark.parametrize("tau", [0.0, 8.0])
+def test_correction_modes_agree_bit_for_bit(shape, tau):
+    """The softmax warp rescaling its own rows and the correction warpgroup
+    doing it compute the same products in the same order."""
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=44, dist="wide")
+    o1, l1 = _run(q, k, v, causal, tau=tau, correction_warpgroup=False)
+    o2, l2 = _run(q, k, v, causal, tau=tau, correction_warpgroup=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_lazy_and_eager_agree_to_bf16_noise():
