@@ -533,7 +533,8 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
         if (j >= tl.nkv[t]) continue;
         trace_mark_lane0<TRACE>(p, kTrMmaPvWait, j, t, iter);
         FA4_PROF_CLK(pm_a);
-        if (!(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
+        if (p.correction_wg &&
+            !(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
           break;
         if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
             !(ok = w.wait_warp(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
@@ -812,8 +813,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
             tc_fence_before_sync();
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bOReady + t));
+        // No o_ready arrival: the P arrival below comes after this warp's
+        // rescale in program order, so the MMA warp waits for P alone.
         if (j > 0) ++n_steps;
 #ifdef FA4_PROF
         pr_t2 = static_cast<unsigned>(clock());
