@@ -459,7 +459,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   // O_t (+)= P_t V; each slice of P is issued once the softmax warps have
   // stored it. `phase` counts this tile's earlier P*V MMAs. Returns false on
   // abort.
-  auto issue_pv = [&](int t, int slot, bool first, int phase) -> bool {
+  auto issue_pv = [&](int t, int slot, bool first, int phase, bool commit_done) -> bool {
     const uint32_t v_lo = ring_lo_v + slot * kSlotStep;
     constexpr int kSlices = FP8 ? 1 : FA4_P_SLICES;   // the FP8 P is released whole
 #pragma unroll
@@ -487,7 +487,10 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
         }
       }
     }
-    mma_commit_warp(bar(L::bPvDone + t));
+    // pv_done is only needed after a tile's last P*V of a work tile (the
+    // epilogue) and, in strict order, before every next S. Any other P*V
+    // has completed once the commit of the S MMA issued behind it arrives.
+    if (commit_done) mma_commit_warp(bar(L::bPvDone + t));
     return true;
   };
   auto wait_slot = [&](int pos) -> bool {
@@ -541,7 +544,8 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
           break;
         tc_fence_after_sync();
         trace_mark_lane0<TRACE>(p, kTrMmaPvGo, j, t, iter);
-        if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t]))) break;
+        if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t], p.strict_order || j + 1 == tl.nkv[t])))
+          break;
         ++n_pv[t];
         FA4_PROF_CLK(pm_b);
         trace_mark_lane0<TRACE>(p, kTrMmaPvIssued, j, t, iter);
@@ -637,10 +641,10 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bCDone + 2 * t + buf));
         if (flagged) {
-          // This 32-row group's reference max moved: O_t <- alpha * O_t once
-          // the previous P*V into O_t has completed, then release the group.
-          if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
-            return;
+          // This 32-row group's reference max moved: O_t <- alpha * O_t, then
+          // release the group. The previous P*V into O_t has completed: the
+          // S MMA issued behind it had completed before the softmax warps
+          // arrived on p_full.
           tc_fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
@@ -725,6 +729,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   unsigned pr_acc[5] = {0, 0, 0, 0, 0}, pr_prev_arrived = 0, pr_n = 0;
 #endif
   int n_step = 0;               // steps of this query tile over all work tiles
+  int n_fin = 0;                // work tiles in which this query tile saw keys
   bool ok = true;
   int iter = 0;
   if (p.test_stall_cycles > 0)   // diagnostic: a wait nothing ends
@@ -782,7 +787,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
 #ifdef FA4_PROF
     unsigned pr_t2 = 0;
 #endif
-    bool inline_ok = true;
     auto release = [&](float m_cand, bool warp_need) {
       if (tracer) trace_mark<TRACE>(p, kTrSmCDone, j, t, iter);
       if (tracer) trace_mark<TRACE>(p, kTrSmMaxDone, j, t, iter);
@@ -793,13 +797,10 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
           if (m_cand != -INFINITY) m_ref = m_cand;
           if (j > 0) {
             ++n_rescaled;
-            // O_t <- alpha * O_t for this warp's rows, once the previous P*V
-            // into O_t has completed
-            if (!w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)) {
-              inline_ok = false;
-              return;
-            }
-            tc_fence_after_sync();
+            // O_t <- alpha * O_t for this warp's rows. The previous P*V into
+            // O_t has completed: the S MMA issued behind it, whose commit this
+            // step waited for, tracks it too.
+
 #pragma unroll 1
             for (int c = 0; c < D / 16; ++c) {
               uint32_t x[16];
@@ -856,7 +857,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
       release(m_cand, __any_sync(0xffffffffu, m_cand > m_ref + p.tau));
       exp_pass<EMU_PAIR_PERIOD, FP8>(s, c2, neg_ref(), pk, tot);
     }
-    if (!(ok = inline_ok)) break;
     FA4_PROF_CLK(pr_t3);
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
     // P goes to the first kPCols columns of S_t, released to the P*V MMAs
@@ -915,7 +915,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   __nv_bfloat16* orow = p.o + orow_idx * static_cast<int64_t>(D);
   float* prow = p.o_part + (part_off + orow_idx) * static_cast<int64_t>(D);
   if (n > 0) {
-    if (!(ok = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t)))
+    // one pv_done commit per work tile (per step in strict order)
+    const uint32_t pv_par = p.strict_order ? static_cast<uint32_t>(n_step - 1) & 1u
+                                           : static_cast<uint32_t>(n_fin) & 1u;
+    ++n_fin;
+    if (!(ok = w.wait(bar(L::bPvDone + t), pv_par, L::bPvDone + t)))
       break;
     tc_fence_after_sync();
 #pragma unroll
