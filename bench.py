@@ -73,16 +73,25 @@ def max_over_ranks(values: List[float], dist, device) -> List[float]:
     return t.tolist()
 
 
-def kernel_sources_hash() -> str:
-    """Hash of the kernel sources; a stored ncu traffic figure only applies
-    to the build it was measured on."""
+# Source files each kernel's code and launch depend on.
+KERNEL_SOURCES = {
+    "fa4_fwd_kernel": ["fa4_fwd_kernel.cuh", "fa4_ptx.cuh", "fa4_exp2.cuh", "fa4_launch.cuh",
+                       "fa4_internal.h", "fa4_api.cu", "fa4_fwd_d128.cu", "fa4_fwd_d64.cu",
+                       "fa4_fwd_fp8.cu", "fa4_merge.cu"],
+    "fa4_bwd_kernel": ["fa4_bwd_kernel.cuh", "fa4_bwd.cu", "fa4_fwd_kernel.cuh", "fa4_ptx.cuh",
+                       "fa4_exp2.cuh", "fa4_internal.h", "fa4_api.cu"],
+}
+
+
+def kernel_sources_hash(kernel: str = KERNEL_NAME) -> str:
+    """Hash of the sources a kernel depends on; a stored ncu traffic figure
+    only applies to the build it was measured on."""
     csrc = os.path.join(ROOT, "attention_forward_fa4_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode())
-                h.update(fh.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -95,7 +104,7 @@ def stored_traffic(workload_name: str, kernel: str = KERNEL_NAME) -> Optional[di
     text = open(path).read()
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_h = re.search(r"kernel_sources_hash:\s*([0-9a-f]+)", text)
-    if not m_b or not m_h or m_h.group(1) != kernel_sources_hash():
+    if not m_b or not m_h or m_h.group(1) != kernel_sources_hash(kernel):
         return None
     return {"bytes": float(m_b.group(1)), "source": os.path.relpath(path, ROOT)}
 
@@ -109,6 +118,35 @@ def measured_peaks() -> dict:
         return d
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "_source": "fallback"}
+
+
+def fp8_gemm_peak_tflops(dev) -> Optional[float]:
+    """Burst rate of a dense e4m3 GEMM (torch._scaled_mm, cuBLASLt) at
+    8192^3 on this GPU: the FP8 counterpart of MEASURED_PEAKS' BF16 figure.
+    Best of 10 timed calls after 3 warm-ups; None if the call is unavailable."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        def fn():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record()
+            fn()
+            s1.record()
+            torch.cuda.synchronize()
+            best = min(best, s0.elapsed_time(s1))
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
 
 
 def table1_cycles(M: int, N: int, d: int, flops_per_clk: float = 8192.0,
@@ -450,6 +488,38 @@ def run_ours(args, w: workloads.Workload) -> None:
         raise SystemExit("end-to-end output differs from the device-resident run")
     h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
     d2h = o.numel() * 2 + lse.numel() * 4
+
+    # ---- copy roofline of the end-to-end step: the same host<->device copies
+    # (one per tensor, same pinned buffers, two alternating streams) with no
+    # kernel in between
+    ins_h = [q_p, k_p, v_p] + ([o_bp, lse_bp, do_p] if bwd else [])
+    outs_h = [grads_pp[b] for b in range(2)] if bwd else [[o_pp[b], lse_pp[b]] for b in range(2)]
+    outs_src = [dq, dk, dv] if bwd else [o, lse]
+    ins_dev = [[torch.empty(t.shape, dtype=t.dtype, device=dev) for t in ins_h] for _ in range(2)]
+    outs_dev = [[torch.empty_like(t) for t in outs_src] for _ in range(2)]
+    torch.cuda.synchronize()
+    c_start = torch.cuda.Event(enable_timing=True)
+    c_end = torch.cuda.Event(enable_timing=True)
+    main = torch.cuda.current_stream(dev)
+    c_start.record(main)
+    for st in streams:
+        st.wait_event(c_start)
+    for i in range(e2e_steps):
+        b = i % 2
+        with torch.cuda.stream(streams[b]):
+            for dst, src in zip(ins_dev[b], ins_h):
+                dst.copy_(src, non_blocking=True)
+            for dst, src in zip(outs_h[b], outs_dev[b]):
+                dst.copy_(src, non_blocking=True)
+    for st in streams:
+        ev = torch.cuda.Event()
+        ev.record(st)
+        main.wait_event(ev)
+    c_end.record(main)
+    torch.cuda.synchronize()
+    copy_ms = c_start.elapsed_time(c_end)
+    del ins_dev, outs_dev
+
     if bwd:
         h2d += o.numel() * 2 + lse.numel() * 4 + dout.numel() * 2
         d2h = (dq.numel() + dk.numel() + dv.numel()) * 2
@@ -463,9 +533,37 @@ def run_ours(args, w: workloads.Workload) -> None:
     per_launch_ms = kernel_ms / args.steps
     achieved = flops_rank_step / (per_launch_ms * 1e-3) / 1e12
     peaks = measured_peaks()
-    peak = float(peaks.get("bf16_tflops", 1900.0)) * (FP8_OVER_BF16 if fp8 else 1.0)
-    peak_source = f"{peaks['_source']} bf16_tflops (burst)" + (
-        f" x {FP8_OVER_BF16:g} (nominal FP8:BF16 dense ratio)" if fp8 else "")
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_source = f"{peaks['_source']} bf16_tflops (burst)"
+    if fp8:
+        fp8_peak = fp8_gemm_peak_tflops(dev) if rank == 0 else None
+        if fp8_peak:
+            peak = fp8_peak
+            peak_source = "measured here: e4m3 GEMM 8192^3 (torch._scaled_mm), best of 10"
+        else:
+            peak *= FP8_OVER_BF16
+            peak_source += f" x {FP8_OVER_BF16:g} (nominal FP8:BF16 dense ratio)"
+
+    # lazy-rescale counts of this workload: 32-row-group steps (after each
+    # tile's first key block) that rescaled the output, at tau and at 0
+    rescale = None
+    if not bwd and not args.no_rescale_stats:
+        cnt = {}
+        for tau in (args.tau, 0.0):
+            stats = torch.zeros(2, dtype=torch.int64, device=dev)
+            if fp8:
+                fa4.fwd_fp8_into(q, k, v, o, lse, qs, ks, vs, w.causal, w.scale, tau=tau,
+                                 rescale_stats=stats, stream=stream)
+            else:
+                fa4.fwd_into(q, k, v, o, lse, w.causal, w.scale, tau=tau, rescale_stats=stats,
+                             stream=stream, **{k_: v_ for k_, v_ in kw.items() if k_ != "tau"})
+            torch.cuda.synchronize()
+            cnt[tau] = stats.cpu().tolist()
+        r_tau, steps = cnt[args.tau]
+        r_eager = cnt[0.0][0]
+        rescale = {"tau": args.tau, "row_group_steps": steps, "rescales": r_tau,
+                   "rescales_at_tau_0": r_eager,
+                   "fewer_by": (r_eager / r_tau) if r_tau else None}
     traffic = (stored_traffic(w.name, "fa4_bwd_kernel") if bwd else
                stored_traffic(w.name + ("_fp8" if fp8 else "")
                               + (f"_split{args.num_splits}" if args.num_splits else "")))
@@ -515,8 +613,17 @@ def run_ours(args, w: workloads.Workload) -> None:
                                                w_rank.hbm_bytes_fp8 if fp8 else w_rank.hbm_bytes)},
             "cpu_baseline": cpu,
             "clocks": clocks,
+            "rescale_stats": rescale,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "copy_roofline": {
+                        "what": ("the step's host<->device copies alone: same tensors, pinned "
+                                 "buffers and two alternating streams, no kernel"),
+                        "bytes_per_step": h2d + d2h,
+                        "ms_per_step": copy_ms / e2e_steps,
+                        "gbs": (h2d + d2h) * e2e_steps / (copy_ms * 1e-3) / 1e9,
+                        "e2e_ms_per_step": e2e_ms / e2e_steps,
+                        "frac": copy_ms / e2e_ms},
                     "api": ("fa4_fwd_host (pinned host buffers, copies inside the call), "
                             "2 streams alternating" if host_api else
                             "torch copies from pinned host buffers around the call, "
@@ -550,6 +657,7 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-rescale-stats", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
