@@ -331,24 +331,31 @@ __device__ __forceinline__ void bwd_compute_role(const CUtensorMap* tm_dq, uint3
       tmem_wait_ld_x32(sv);
       tmem_wait_ld_x32(dv);
       uint32_t pk[16], dk[16];
+      // Pairs of entries on the paired FP32 instructions (FFMA2 / FADD2 /
+      // FMUL2): p = 2^(c s - LSE2), dS = p (dP - Delta); masked entries 0.
+      const float2 c22 = make_float2(c2, c2);
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
         const float4 l4 = lse4[8 * c + e4];
         const float4 d4 = delta4[8 * c + e4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pe[4], de[4];
+        const float2 nl[2] = {make_float2(-l4.x, -l4.y), make_float2(-l4.z, -l4.w)};
+        const float2 nd[2] = {make_float2(-d4.x, -d4.y), make_float2(-d4.z, -d4.w)};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = 4 * e4 + u;
-          float pv = ex2_mufu(__uint_as_float(sv[e]) * c2 - lv[u]);
-          if (!row_live || (!all_visible && kabs > q0 + 32 * c + e + shift)) pv = 0.0f;
-          pe[u] = pv;
-          de[u] = pv * (__uint_as_float(dv[e]) - dl[u]);
+        for (int u = 0; u < 2; ++u) {
+          const int e = 4 * e4 + 2 * u;
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22, nl[u]);
+          float2 pv = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+          if (!row_live) pv = make_float2(0.0f, 0.0f);
+          if (!all_visible) {
+            const int lim = kabs - shift - q0 - 32 * c;   // entries e with e < lim are masked
+            if (e < lim) pv.x = 0.0f;
+            if (e + 1 < lim) pv.y = 0.0f;
+          }
+          const float2 t = __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd[u]);
+          const float2 de = __fmul2_rn(pv, t);
+          pk[2 * e4 + u] = pack_bf16x2(pv.x, pv.y);
+          dk[2 * e4 + u] = pack_bf16x2(de.x, de.y);
         }
-        pk[2 * e4] = pack_bf16x2(pe[0], pe[1]);
-        pk[2 * e4 + 1] = pack_bf16x2(pe[2], pe[3]);
-        dk[2 * e4] = pack_bf16x2(de[0], de[1]);
-        dk[2 * e4 + 1] = pack_bf16x2(de[2], de[3]);
       }
       // P^T over S^T and dS^T over dP^T, in the first 16 of this chunk's own
       // 32 columns (already read; the other warp of the lane quarter works
