@@ -97,9 +97,9 @@ int sm_count(int dev) {
   return n;
 }
 
-// [B, S, H, d] BF16 as a 4-D tensor (d, H, S, B); box = 64 columns x 128 rows
-// of one head, 128-byte swizzle (one swizzle row = 64 BF16).
-bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+// [B, S, H, d] BF16 as a 4-D tensor (d, H, S, B); box = 64 columns x `rows`
+// rows of one head, 128-byte swizzle (one swizzle row = 64 BF16).
+bool make_map_rows(CUtensorMap* map, const void* ptr, int B, int S, int H, int d, int rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
@@ -107,11 +107,14 @@ bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(H) * d * 2,
                                  static_cast<cuuint64_t>(S) * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+  return make_map_rows(map, ptr, B, S, H, d, kBM);
 }
 
 // e4m3 [B, S, H, d] tensor as a 4-D map: a 128-column x 128-row box (128
@@ -131,8 +134,8 @@ bool make_map_u8(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) 
 }
 
 // fp32 [B, S, H, d] tensor (the backward's dQ accumulator) as a 4-D map with
-// a 32-column x 128-row box and 128-byte swizzle (32 fp32 = 128 bytes).
-bool make_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int d) {
+// a 32-column x `rows`-row box and 128-byte swizzle (32 fp32 = 128 bytes).
+bool make_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int d, int rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
@@ -140,7 +143,7 @@ bool make_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int d)
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(H) * d * 4,
                                  static_cast<cuuint64_t>(S) * H * d * 4};
-  const cuuint32_t box[4] = {32, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t box[4] = {32, 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box,
              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -470,7 +473,8 @@ uint64_t fa4_fwd_splitkv_workspace_bytes(int B, int Hq, int Sq, int d, int num_s
 uint64_t fa4_bwd_workspace_bytes(int B, int Hq, int Sq, int d) {
   if (B < 0 || Hq < 0 || Sq < 0 || d < 0) return 0;
   const uint64_t sq_pad = (static_cast<uint64_t>(Sq) + 127) / 128 * 128;
-  const uint64_t turns = (static_cast<uint64_t>(B) * Hq * (sq_pad / 128) * 4 + 15) / 16 * 16;
+  // one int per (batch, query head, 64-query block)
+  const uint64_t turns = (static_cast<uint64_t>(B) * Hq * (sq_pad / 64) * 4 + 15) / 16 * 16;
   // + 16 bytes: the deterministic mode's CTA ticket counter
   return static_cast<uint64_t>(B) * Sq * Hq * d * 4 + 2ull * B * Hq * sq_pad * 4 + turns + 16;
 }
@@ -544,15 +548,18 @@ fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o
     return FA4_OK;
   }
   float* dq_acc = static_cast<float*>(workspace);
+  // Q and dO move in blocks of 64 query rows at head dim 128 and of 128 at
+  // 64, dQ reduce-adds in blocks of 32 and 128 rows; K and V in blocks of
+  // 128 key rows.
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_map(&tq, q, B, Sq, Hq, d) || !make_map(&tk, k, B, Sk, Hkv, d) ||
-      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map(&tdo, dout, B, Sq, Hq, d) ||
-      !make_map_f32(&tdq, dq_acc, B, Sq, Hq, d))
+  if (!make_map_rows(&tq, q, B, Sq, Hq, d, d == 128 ? 64 : kBM) || !make_map(&tk, k, B, Sk, Hkv, d) ||
+      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map_rows(&tdo, dout, B, Sq, Hq, d, d == 128 ? 64 : kBM) ||
+      !make_map_f32(&tdq, dq_acc, B, Sq, Hq, d, d == 128 ? 32 : kBM))
     return FA4_ERR_CUDA;
   float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
   float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);
   int* turns = reinterpret_cast<int*>(delta + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128));
-  const uint64_t turn_ints = (static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128) * 4 + 15) / 16 * 4;
+  const uint64_t turn_ints = (static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 2) * 4 + 15) / 16 * 4;
   int* ticket = turns + turn_ints;
   cudaError_t err = launch_bwd(tq, tk, tv, tdo, tdq, static_cast<const __nv_bfloat16*>(o),
                                static_cast<const __nv_bfloat16*>(dout), lse,

@@ -1,10 +1,12 @@
 // fa4_bwd.cu -- host launch of the attention backward: a preprocessing
 // kernel (Delta = rowsum(dO o O), LSE in log2 units, both padded to whole
-// 128-row blocks), the tcgen05 main kernel (fa4_bwd_kernel.cuh), and the
-// conversion of the fp32 dQ accumulator to BF16.
+// 128-row blocks), the tcgen05 main kernel (fa4_bwd_kernel.cuh at head dim
+// 64, fa4_bwd_q64.cuh at 128), and the conversion of the fp32 dQ
+// accumulator to BF16.
 #include <cuda_bf16.h>
 
 #include "fa4_bwd_kernel.cuh"
+#include "fa4_bwd_q64.cuh"
 #include "fa4_internal.h"
 
 namespace fa4 {
@@ -73,6 +75,18 @@ cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   return cudaGetLastError();
 }
 
+template <bool CAUSAL>
+cudaError_t launch_q64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                       unsigned grid, cudaStream_t s) {
+  constexpr int kSmem = BwdQ64Smem::kAlloc;
+  constexpr auto kernel = fa4_bwd_q64_kernel<CAUSAL>;
+  cudaError_t err = set_smem_once<kernel>(kSmem);
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, kBwdQ64Threads, kSmem, s>>>(tq, tk, tv, tdo, tdq, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -87,7 +101,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   cudaError_t err = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(dq_elems) * 4, s);
   if (err != cudaSuccess) return err;
   if (dq_turn &&
-      (err = cudaMemsetAsync(dq_turn, 0, static_cast<size_t>(B) * Hq * (Sq_pad / 128) * 4, s)) != cudaSuccess)
+      (err = cudaMemsetAsync(dq_turn, 0, static_cast<size_t>(B) * Hq * (Sq_pad / 64) * 4, s)) != cudaSuccess)
     return err;
   if (cta_ticket && (err = cudaMemsetAsync(cta_ticket, 0, sizeof(int), s)) != cudaSuccess) return err;
   const int64_t prep_rows = static_cast<int64_t>(B) * Hq * Sq_pad;
@@ -122,8 +136,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     err = causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)
                  : launch_main<64, false>(tq, tk, tv, tdo, tdq, p, grid, s);
   else
-    err = causal ? launch_main<128, true>(tq, tk, tv, tdo, tdq, p, grid, s)
-                 : launch_main<128, false>(tq, tk, tv, tdo, tdq, p, grid, s);
+    err = causal ? launch_q64<true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                 : launch_q64<false>(tq, tk, tv, tdo, tdq, p, grid, s);
   if (err != cudaSuccess) return err;
 
   const int64_t n4 = dq_elems / 4;

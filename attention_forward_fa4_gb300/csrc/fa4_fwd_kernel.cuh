@@ -82,7 +82,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimitCycles = 1ll << 30;
 
 enum : unsigned { kStatusTimeout = 5u, kStatusMisalignedSmem = 3u };
-enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3, kRoleFlush = 4 };
+enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3, kRoleFlush = 4, kRoleDqRead = 5 };
 
 struct FwdParams {
   __nv_bfloat16* o;            // [B, Sq, Hq, D]

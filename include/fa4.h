@@ -226,7 +226,7 @@ fa4_status fa4_fwd_fp8(const void *q, const void *k, const void *v, void *o, flo
  *                    least fa4_bwd_workspace_bytes(B, Hq, Sq, d) bytes: the
  *                    fp32 dQ accumulator [B, Sq, Hq, d], then LSE log2(e)
  *                    and rowsum(dO o O), each [B, Hq, Sq rounded up to 128],
- *                    then one int per (batch, query head, query block)
+ *                    then one int per (batch, query head, 64-query block)
  *                    (padded to 16 bytes), then one int (the CTA ticket).
  *   other arguments and rules as fa4_fwd; dq, dk, dv and the workspace
  *   must not overlap each other or any input.
@@ -338,7 +338,8 @@ fa4_status fa4_fwd_splitkv_static(const void *q, const void *k, const void *v, v
  * not 1 KB aligned (it then exits without work). `detail`
  * (may be NULL) receives 4 words: the error code, the waiting role
  * (0 load, 1 mma, 2 softmax -- the backward's compute warps --,
- * 3 correction, 4 the backward's dQ flush warp), the barrier id (an index
+ * 3 correction, 4 the backward's dQ flush warp, 5 the head-dim-128
+ * backward's dQ^T read-out warps), the barrier id (an index
  * into the kernel's own barrier table) and the block index. When `clear`
  * is non-zero the word is reset to FA4_OK.
  * Returns FA4_ERR_CUDA if the device cannot be reached.

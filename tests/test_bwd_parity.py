@@ -64,6 +64,10 @@ CASES = [
     (1, 1, 1, 1, 1, 128, False),        # single query, single key
     (1, 3, 3, 64, 5, 64, False),        # fewer keys than a block
     (1, 4, 2, 1024, 1024, 128, True),   # several blocks each way
+    (1, 2, 1, 320, 320, 128, True),     # GQA; key blocks with 2 and 4 query steps of 64
+    (2, 4, 4, 190, 333, 128, False),    # ragged both ways, 3 query steps of 64
+    (1, 2, 2, 64, 256, 128, True),      # one 64-query step per head
+    (1, 8, 1, 96, 128, 128, False),     # group of 8: 16 steps through one key block
 ]
 
 
