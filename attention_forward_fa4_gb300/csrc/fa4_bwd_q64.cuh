@@ -67,11 +67,11 @@ struct BwdQ64Smem {
   static constexpr int kLd = kStage0 + kStages * kStageBytes;   // per stage LSE2[64], Delta[64]
   static constexpr int kBars = kLd + kStages * 512;
   // kv; per stage full (Q, dO, LSE2, Delta) and empty (after the dK MMA);
-  // per buffer sdp (S^T and dP^T committed); p_ready (P^T, dS^T written),
+  // per buffer s / dp (S^T, dP^T committed); p_ready (P^T, dS^T written),
   // dq_full / dq_free (dQ^T committed / read out), acc (all MMAs done); per
   // staging slot full / free (handed to / back from the flush warp)
-  static constexpr int bKv = 0, bFull = 1, bEmpty = bFull + kStages, bSdp = bEmpty + kStages,
-                       bPReady = bSdp + 2, bDqFull = bPReady + 1, bDqFree = bDqFull + 1,
+  static constexpr int bKv = 0, bFull = 1, bEmpty = bFull + kStages, bS = bEmpty + kStages,
+                       bDP = bS + 2, bPReady = bDP + 2, bDqFull = bPReady + 1, bDqFree = bDqFull + 1,
                        bAcc = bDqFree + 1, bSlotFull = bAcc + 1, bSlotFree = bSlotFull + kSlots,
                        kNumBars = bSlotFree + kSlots;
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag, work number
@@ -173,31 +173,25 @@ __device__ __forceinline__ void bwd_q64_mma_role(uint32_t sbase, uint32_t tmem, 
   const uint32_t k_mn = desc_lo_sw128(sbase + L::kK, L::kKvPanel);
   // dS as an MN-major B operand: N = the step's 64 queries (one swizzle row)
   const uint32_t ds_mn = desc_lo_sw128(sbase + L::kDS, L::kKvPanel);
-  auto issue_sdp = [&](int s) {
-    const int b = s & 1;
-    const uint32_t q_lo = desc_lo_sw128(sbase + L::stage(s) + L::kQ, 16);
-    const uint32_t do_lo = desc_lo_sw128(sbase + L::stage(s) + L::kDO, 16);
+  // S^T = K Q^T or dP^T = V dO^T of step s into buffer s % 2, then a commit
+  // to that product's barrier
+  auto issue_kq = [&](int s, uint32_t a_lo, int col, int opnd, int done) {
+    const uint32_t b_lo = desc_lo_sw128(sbase + L::stage(s) + opnd, 16);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t a_off = ((kk >> 2) * L::kKvPanel + (kk & 3) * 32) >> 4;
       const uint32_t b_off = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
-      mma_ss_lohi_warp(tmem + L::kColS + 64 * b, k_lo + a_off, kHi, q_lo + b_off, kHi, kIdescS,
+      mma_ss_lohi_warp(tmem + col + 64 * (s & 1), a_lo + a_off, kHi, b_lo + b_off, kHi, kIdescS,
                        kk > 0 ? 1u : 0u);
     }
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a_off = ((kk >> 2) * L::kKvPanel + (kk & 3) * 32) >> 4;
-      const uint32_t b_off = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
-      mma_ss_lohi_warp(tmem + L::kColDP + 64 * b, v_lo + a_off, kHi, do_lo + b_off, kHi, kIdescS,
-                       kk > 0 ? 1u : 0u);
-    }
-    mma_commit_warp(bar(L::bSdp + b));
+    mma_commit_warp(bar(done + (s & 1)));
   };
   bool ok = w.wait_warp(bar(L::bKv), 0u, L::bKv);
   for (int s = 0; ok && s < 2 && s < wk.steps; ++s) {
     if (!(ok = w.wait_warp(bar(L::bFull + s), 0u, L::bFull + s))) break;
     tc_fence_after_sync();
-    issue_sdp(s);
+    issue_kq(s, k_lo, L::kColS, L::kQ, L::bS);
+    issue_kq(s, v_lo, L::kColDP, L::kDO, L::bDP);
   }
   for (int s = 0; ok && s < wk.steps; ++s) {
     const int b = s & 1;
@@ -224,19 +218,24 @@ __device__ __forceinline__ void bwd_q64_mma_role(uint32_t sbase, uint32_t tmem, 
       mma_ts_lohi_warp(tmem + L::kColDK, pcol + 32 * (kk >> 1) + 16 + 8 * (kk & 1), q_mn + kk * (2048 >> 4),
                        kHi, kIdescTs, (s > 0 || kk > 0) ? 1u : 0u);
     mma_commit_warp(bar(L::bEmpty + st));   // the stage's Q and dO read
-    // Step s + 2 reuses this step's columns: S^T once dV and dK (issued
-    // above, executed in order) have read P^T and dS^T, dP^T once the
+    // Step s + 2 reuses this step's columns: S^T at once (dV and dK, issued
+    // above, execute first and read P^T and dS^T there), dP^T once the
     // read-out warps have read dQ^T. Waiting for the read-out on every step
     // (the last two too) also keeps dq_full from completing a second phase
     // before those warps have seen the first.
-    if (!(ok = w.wait_warp(bar(L::bDqFree), static_cast<uint32_t>(s) & 1u, L::bDqFree))) break;
-    if (s + 2 < wk.steps) {
+    const bool next = s + 2 < wk.steps;
+    if (next) {
       const int st2 = (s + 2) % L::kStages;
       if (!(ok = w.wait_warp(bar(L::bFull + st2), static_cast<uint32_t>((s + 2) / L::kStages) & 1u,
                              L::bFull + st2)))
         break;
       tc_fence_after_sync();
-      issue_sdp(s + 2);
+      issue_kq(s + 2, k_lo, L::kColS, L::kQ, L::bS);
+    }
+    if (!(ok = w.wait_warp(bar(L::bDqFree), static_cast<uint32_t>(s) & 1u, L::bDqFree))) break;
+    if (next) {
+      tc_fence_after_sync();
+      issue_kq(s + 2, v_lo, L::kColDP, L::kDO, L::bDP);
     }
   }
   // Every MMA issued above has completed once this commit arrives (the
@@ -246,6 +245,32 @@ __device__ __forceinline__ void bwd_q64_mma_role(uint32_t sbase, uint32_t tmem, 
 }
 
 // ------------------------------------------------------------ compute warps
+// p = 2^(c s - LSE2) for one thread's 32 entries (pairs on FFMA2); with MASK,
+// 0 for a key row past Sk and for entries e < lim (above the causal
+// diagonal).
+template <bool MASK>
+__device__ __forceinline__ void bwd_q64_p(const uint32_t (&sv)[32], const float4* lse4, float c2,
+                                          bool row_live, int lim, float (&pv)[32]) {
+  const float2 c22 = make_float2(c2, c2);
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 l4 = lse4[e4];
+    const float2 nl[2] = {make_float2(-l4.x, -l4.y), make_float2(-l4.z, -l4.w)};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = 4 * e4 + 2 * u;
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22, nl[u]);
+      float a = ex2_mufu(x.x), bb = ex2_mufu(x.y);
+      if (MASK) {
+        if (!row_live || e < lim) a = 0.0f;
+        if (!row_live || e + 1 < lim) bb = 0.0f;
+      }
+      pv[e] = a;
+      pv[e + 1] = bb;
+    }
+  }
+}
+
 // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
 // queries 32 (w / 4) .. + 31 of each step. At the end it writes half of the
 // columns of its rows of dK and dV.
@@ -264,6 +289,7 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
   const int shift = p.Sk - p.Sq;
   const int per_head = wk.n_qb - wk.qb0;
   const bool row_live = kabs < p.Sk;
+  const bool rows_live = wk.k0 + 128 <= p.Sk;          // every key row of the block exists
   bool ok = true;
   for (int s = 0; s < wk.steps; ++s) {
     const int b = s & 1;
@@ -273,45 +299,46 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
     const float4* delta4 = reinterpret_cast<const float4*>(smem + L::delta(s)) + 8 * ch;
     if (!(ok = w.wait(bar(L::bFull + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bFull + st)))
       break;
-    if (!(ok = w.wait(bar(L::bSdp + b), static_cast<uint32_t>(s >> 1) & 1u, L::bSdp + b))) break;
+    if (!(ok = w.wait(bar(L::bS + b), static_cast<uint32_t>(s >> 1) & 1u, L::bS + b))) break;
     tc_fence_after_sync();
     const uint32_t scol = lane_base + L::kColS + 64 * b + 32 * ch;
     const uint32_t dcol = lane_base + L::kColDP + 64 * b + 32 * ch;
-    uint32_t sv[32], dv[32];
+    uint32_t sv[32];
     tmem_ld_x32(scol, sv);
-    tmem_ld_x32(dcol, dv);
     tmem_wait_ld_x32(sv);
-    tmem_wait_ld_x32(dv);
-    // tile-uniform: every (key, query) pair of the step is visible
-    const bool all_visible = !CAUSAL || (wk.k0 + 127 <= q0 + shift);
-    const int lim = kabs - shift - q0 - 32 * ch;        // entries e < lim are masked
+    // P = 2^(c S - LSE2) while dP^T is still being formed; masked entries
+    // (keys past Sk, and above the causal diagonal) only on tiles that have
+    // any, which is tile-uniform
+    float pv[32];
+    const bool masked = !rows_live || (CAUSAL && wk.k0 + 127 > q0 + shift);
+    if (masked)
+      bwd_q64_p<true>(sv, lse4, c2, row_live, CAUSAL ? kabs - shift - q0 - 32 * ch : -1, pv);
+    else
+      bwd_q64_p<false>(sv, lse4, c2, true, 0, pv);
     uint32_t pk[16], dk[16];
-    const float2 c22 = make_float2(c2, c2);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+    // P^T into the first 16 of this warp's own (already read) S^T columns
+    tmem_st_x16(scol, pk);
+    if (!(ok = w.wait(bar(L::bDP + b), static_cast<uint32_t>(s >> 1) & 1u, L::bDP + b))) break;
+    tc_fence_after_sync();
+    uint32_t dv[32];
+    tmem_ld_x32(dcol, dv);
+    tmem_wait_ld_x32(dv);
+    // dS = P (dP - Delta) on paired FP32 instructions
 #pragma unroll
     for (int e4 = 0; e4 < 8; ++e4) {
-      const float4 l4 = lse4[e4];
       const float4 d4 = delta4[e4];
-      const float2 nl[2] = {make_float2(-l4.x, -l4.y), make_float2(-l4.z, -l4.w)};
       const float2 nd[2] = {make_float2(-d4.x, -d4.y), make_float2(-d4.z, -d4.w)};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int e = 4 * e4 + 2 * u;
-        // p = 2^(c s - LSE2), dS = p (dP - Delta) on paired FP32 instructions
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22, nl[u]);
-        float2 pv = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-        if (!row_live) pv = make_float2(0.0f, 0.0f);
-        if (!all_visible) {
-          if (e < lim) pv.x = 0.0f;
-          if (e + 1 < lim) pv.y = 0.0f;
-        }
         const float2 t = __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd[u]);
-        const float2 de = __fmul2_rn(pv, t);
-        pk[2 * e4 + u] = pack_bf16x2(pv.x, pv.y);
+        const float2 de = __fmul2_rn(make_float2(pv[e], pv[e + 1]), t);
         dk[2 * e4 + u] = pack_bf16x2(de.x, de.y);
       }
     }
-    // P^T and dS^T into this warp's own (already read) S^T columns
-    tmem_st_x16(scol, pk);
+    // dS^T into the other 16
     tmem_st_x16(scol + 16, dk);
     // dS for the dQ^T MMA: row = key, the step's 64 queries in one 128-byte
     // swizzle row (16-byte chunk index XOR row within its 8-row group), once
@@ -517,8 +544,10 @@ __global__ void __launch_bounds__(kBwdQ64Threads, 1)
       mbar_init(bar(L::bFull + i), 1);
       mbar_init(bar(L::bEmpty + i), 1);
     }
-    mbar_init(bar(L::bSdp), 1);
-    mbar_init(bar(L::bSdp + 1), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::bS + i), 1);
+      mbar_init(bar(L::bDP + i), 1);
+    }
     mbar_init(bar(L::bPReady), 256);
     mbar_init(bar(L::bDqFull), 1);
     mbar_init(bar(L::bDqFree), 128);
