@@ -87,9 +87,16 @@ struct BwdQ64Smem {
 template <bool CAUSAL>
 __device__ __forceinline__ BwdWork bwd_q64_work(const BwdParams& p, int id) {
   BwdWork w;
+  // Causal (and deterministic mode): key block outermost, so the longest
+  // CTAs (the first key blocks see the most queries) start first and the
+  // grid ends on short ones; in deterministic mode this also means every
+  // CTA whose turn comes earlier is already running. Otherwise the key
+  // blocks of one (batch, kv head) sit side by side (their CTAs share Q and
+  // dO in L2).
   const int n_bg = p.B * p.Hkv;
-  const int kb = p.dq_turn ? id / n_bg : id % p.n_kblk;
-  const int bg = p.dq_turn ? id % n_bg : id / p.n_kblk;
+  const bool kb_major = CAUSAL || p.dq_turn;
+  const int kb = kb_major ? id / n_bg : id % p.n_kblk;
+  const int bg = kb_major ? id % n_bg : id / p.n_kblk;
   w.b = bg / p.Hkv;
   w.g = bg - w.b * p.Hkv;
   w.k0 = kb * 128;
