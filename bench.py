@@ -356,7 +356,8 @@ def run_ours(args, w: workloads.Workload) -> None:
         st = stream if st is None else st
         if bwd:
             fa4.bwd_into(S["q"], S["k"], S["v"], S["o"], S["dout"], S["lse"], S["dq"], S["dk"],
-                         S["dv"], w.causal, w.scale, workspace=S["wsb"], stream=st)
+                         S["dv"], w.causal, w.scale, deterministic=args.deterministic,
+                         workspace=S["wsb"], stream=st)
         elif fp8:
             fa4.fwd_fp8_into(S["q"], S["k"], S["v"], S["o"], S["lse"], qs, ks, vs, w.causal,
                              w.scale, tau=args.tau, stream=st)
@@ -600,7 +601,8 @@ def run_ours(args, w: workloads.Workload) -> None:
                            l2="flushed before every timed launch (256 MiB write)",
                            tau=args.tau, exp2_emulation=args.exp2_emulation,
                            num_splits=args.num_splits, precision=args.precision,
-                           **{"pass": args.pass_}),
+                           **{"pass": args.pass_},
+                           **({"deterministic": args.deterministic} if bwd else {})),
             "pct_of_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             **({"pct_of_4500_tflops": 100.0 * value / world / (2 * NOMINAL_BF16_TFLOPS)}
                if fp8 else {}),
@@ -653,6 +655,8 @@ def main(argv: Optional[List[str]] = None) -> None:
                     help="one softmax entry pair in N through the software 2^x (0: none)")
     ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
                     help="fp8: e4m3 Q, K, V (per-tensor scales) through fa4_fwd_fp8")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward only: dQ tiles added in key-block order (fa4_bwd_ex)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
