@@ -548,13 +548,12 @@ fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o
     return FA4_OK;
   }
   float* dq_acc = static_cast<float*>(workspace);
-  // Q and dO move in blocks of 64 query rows at head dim 128 and of 128 at
-  // 64, dQ reduce-adds in blocks of 32 and 128 rows; K and V in blocks of
-  // 128 key rows.
+  // Q and dO move in blocks of 64 query rows, dQ reduce-adds in blocks of 32
+  // rows at head dim 128 and 64 at 64; K and V in blocks of 128 key rows.
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_map_rows(&tq, q, B, Sq, Hq, d, d == 128 ? 64 : kBM) || !make_map(&tk, k, B, Sk, Hkv, d) ||
-      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map_rows(&tdo, dout, B, Sq, Hq, d, d == 128 ? 64 : kBM) ||
-      !make_map_f32(&tdq, dq_acc, B, Sq, Hq, d, d == 128 ? 32 : kBM))
+  if (!make_map_rows(&tq, q, B, Sq, Hq, d, 64) || !make_map(&tk, k, B, Sk, Hkv, d) ||
+      !make_map(&tv, v, B, Sk, Hkv, d) || !make_map_rows(&tdo, dout, B, Sq, Hq, d, 64) ||
+      !make_map_f32(&tdq, dq_acc, B, Sq, Hq, d, d == 128 ? 32 : 64))
     return FA4_ERR_CUDA;
   float* lse2 = dq_acc + static_cast<uint64_t>(B) * Sq * Hq * d;
   float* delta = lse2 + static_cast<uint64_t>(B) * Hq * ((Sq + 127) / 128 * 128);

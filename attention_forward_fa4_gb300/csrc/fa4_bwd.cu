@@ -1,11 +1,9 @@
 // fa4_bwd.cu -- host launch of the attention backward: a preprocessing
 // kernel (Delta = rowsum(dO o O), LSE in log2 units, both padded to whole
-// 128-row blocks), the tcgen05 main kernel (fa4_bwd_kernel.cuh at head dim
-// 64, fa4_bwd_q64.cuh at 128), and the conversion of the fp32 dQ
-// accumulator to BF16.
+// 128-row blocks), the tcgen05 main kernel (fa4_bwd_q64.cuh), and the
+// conversion of the fp32 dQ accumulator to BF16.
 #include <cuda_bf16.h>
 
-#include "fa4_bwd_kernel.cuh"
 #include "fa4_bwd_q64.cuh"
 #include "fa4_internal.h"
 
@@ -64,23 +62,11 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
-                        unsigned grid, cudaStream_t s) {
-  constexpr int kSmem = BwdSmem<D>::kAlloc;
-  constexpr auto kernel = fa4_bwd_kernel<D, CAUSAL>;
-  cudaError_t err = set_smem_once<kernel>(kSmem);
-  if (err != cudaSuccess) return err;
-  kernel<<<grid, kBwdThreads, kSmem, s>>>(tq, tk, tv, tdo, tdq, p);
-  return cudaGetLastError();
-}
-
-template <bool CAUSAL>
 cudaError_t launch_q64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                        unsigned grid, cudaStream_t s) {
-  constexpr int kSmem = BwdQ64Smem::kAlloc;
-  constexpr auto kernel = fa4_bwd_q64_kernel<CAUSAL>;
+  constexpr int kSmem = BwdQ64Smem<D>::kAlloc;
+  constexpr auto kernel = fa4_bwd_q64_kernel<D, CAUSAL>;
   cudaError_t err = set_smem_once<kernel>(kSmem);
   if (err != cudaSuccess) return err;
   kernel<<<grid, kBwdQ64Threads, kSmem, s>>>(tq, tk, tv, tdo, tdq, p);
@@ -133,11 +119,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.cta_ticket = cta_ticket;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(p.n_kblk) * B * Hkv);
   if (d == 64)
-    err = causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)
-                 : launch_main<64, false>(tq, tk, tv, tdo, tdq, p, grid, s);
+    err = causal ? launch_q64<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                 : launch_q64<64, false>(tq, tk, tv, tdo, tdq, p, grid, s);
   else
-    err = causal ? launch_q64<true>(tq, tk, tv, tdo, tdq, p, grid, s)
-                 : launch_q64<false>(tq, tk, tv, tdo, tdq, p, grid, s);
+    err = causal ? launch_q64<128, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                 : launch_q64<128, false>(tq, tk, tv, tdo, tdq, p, grid, s);
   if (err != cudaSuccess) return err;
 
   const int64_t n4 = dq_elems / 4;

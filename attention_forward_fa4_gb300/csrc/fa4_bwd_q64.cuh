@@ -1,5 +1,5 @@
-// fa4_bwd_q64.cuh -- attention backward at head dim 128 in steps of 64
-// queries, with the next step's S^T / dP^T MMAs overlapping the current
+// fa4_bwd_q64.cuh -- attention backward in steps of 64 queries (head dims
+// 64 and 128), with the next step's S^T / dP^T MMAs overlapping the current
 // step's softmax-side work ("FlashAttention-4: Algorithm and Kernel
 // Pipelining Co-Design for Asymmetric Hardware Scaling", §3.2: five MMAs
 // per tile pair, spread over producer and consumer warps).
@@ -13,12 +13,12 @@
 //   P^T, dS^T (BF16)        compute warps, written over S^T[b]: the warp on
 //                           queries 32 c .. 32 c + 31 puts P^T in columns
 //                           32 c + [0, 16) and dS^T in 32 c + [16, 32)
-//   dQ^T[b] = K^T dS^T      SS MMA, M = 128 (head dim), N = 64 queries,
-//                           A = K read MN-major, B = dS from shared memory;
-//                           into dP^T[b] (already read), issued first so the
-//                           read-out starts early
-//   dV     += P^T dO        TS MMA, A = P^T from TMEM    cols [256, 384)
-//   dK     += dS^T Q        TS MMA, A = dS^T from TMEM   cols [384, 512)
+//   dQ^T[b] = K^T dS^T      SS MMA, M = 128 (head dim; at 64 the K panel
+//                           twice), N = 64 queries, A = K read MN-major, B =
+//                           dS from shared memory; into dP^T[b] (already
+//                           read), issued first so the read-out starts early
+//   dV     += P^T dO        TS MMA, A = P^T from TMEM    cols 256 + [0, D)
+//   dK     += dS^T Q        TS MMA, A = dS^T from TMEM   cols 256 + D + [0, D)
 //
 // With a step's P^T and dS^T both in its S^T columns, the dP^T columns take
 // the dQ^T tile, so a step needs 128 columns and two fit beside dV and dK.
@@ -26,14 +26,14 @@
 // been read out; the tensor core then works on them (and on step s + 1's
 // dV, dK, dQ^T) while the compute warps exponentiate step s + 1.
 //
-// Q, dO, LSE2 and Delta of a step sit in one of three stages (the stage of
-// step s is loaded once step s - 3's dK MMA has read it). The dQ^T tile is
-// read out one head-dimension row per thread and staged transposed, in
-// halves of 32 queries ([32 queries x 32 fp32] blocks, 128-byte swizzle) in
-// a ring of three half-tiles, for bulk tensor reduce-adds into the global
-// fp32 accumulator: a reduce-add reads its 16 KB source in about as long
-// as a step takes, so the next halves are staged while earlier ones are
-// still being read.
+// Q, dO, LSE2 and Delta of a step sit in one of several stages (three at
+// head dim 128, six at 64; the stage of step s is loaded once the dK MMA of
+// the step that used it before has read it). The dQ^T tile is read out one
+// head-dimension row per thread and staged transposed (row = query, 32-
+// column blocks, 128-byte swizzle) in a ring of three units for bulk tensor
+// reduce-adds into the global fp32 accumulator: a reduce-add reads its
+// source in about as long as a step takes, so the next units are staged
+// while earlier ones are still being read.
 //
 // Warps: 0-7 compute (two per TMEM lane quarter, 32 queries each), 8 TMA
 // loads, 9 MMA issue, 10 dQ flush (in deterministic mode in key-block
@@ -42,28 +42,68 @@
 // handed over. Every wait is bounded.
 #pragma once
 
-#include "fa4_bwd_kernel.cuh"
+#include "fa4_fwd_kernel.cuh"
 
 namespace fa4 {
+
+constexpr int kBwdWarpLoad = 8;
+constexpr int kBwdWarpMma = 9;
+constexpr int kBwdWarpFlush = 10;
+
+struct BwdParams {
+  __nv_bfloat16* dk;        // [B, Sk, Hkv, D]
+  __nv_bfloat16* dv;        // [B, Sk, Hkv, D]
+  float* dq_acc;            // [B, Sq, Hq, D] fp32, zeroed; receives scale * dS K
+  const float* lse2;        // [B * Hq][Sq_pad]
+  const float* delta;       // [B * Hq][Sq_pad]
+  int B, Hq, Hkv, Sq, Sk, group, Sq_pad, n_kblk;
+  float scale, scale_log2;
+  unsigned int* status;
+  // Deterministic mode (non-null): one int per (batch, query head, 64-query
+  // block), zeroed; the dQ tile of key block kb is added only once kb
+  // earlier key blocks have added theirs, so the fp32 sums are formed in
+  // the same order on every run. CTAs are then numbered key block first.
+  int* dq_turn;
+  // Deterministic mode: a zeroed counter from which each CTA takes its work
+  // number when it starts, so every lower number belongs to a CTA that is
+  // already running whatever order the hardware dispatched them in.
+  int* cta_ticket;
+};
+
+// The CTA's key block and the query blocks it visits.
+struct BwdWork {
+  int b, g, k0;
+  int qb0, n_qb;      // query blocks [qb0, n_qb) of every head in the group
+  int steps;          // group * (n_qb - qb0)
+};
 
 constexpr int kBwdQ64Threads = 512;
 constexpr int kBwdQ64WarpDq = 12;   // first of the four dQ^T read-out warps
 
+// Head dim 128: two 64-column panels per K, V, Q, dO tile; dQ staged in
+// halves of 32 queries. Head dim 64: one panel, with K loaded twice (the
+// dQ^T MMA's M = 128 then yields the 64 head-dim rows twice, and the
+// read-out warps of the duplicate lanes take the step's other 32 queries);
+// dQ staged per whole step; six Q/dO stages.
+template <int D>
 struct BwdQ64Smem {
-  static constexpr int D = 128;
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int kPanels = D / 64;
   static constexpr int kKvPanel = 128 * 128;            // 128 rows x 64 BF16
   static constexpr int kQPanel = 64 * 128;              // 64 rows x 64 BF16
-  static constexpr int kK = 0;
+  static constexpr int kK = 0;                          // two panels (at D = 64 the same one twice)
   static constexpr int kV = kK + 2 * kKvPanel;
-  static constexpr int kDS = kV + 2 * kKvPanel;         // 128 keys x 64 queries BF16, MN-major
-  static constexpr int kSlots = 3;                      // staging ring of dQ half-tiles
-  static constexpr int kSlotBytes = 32 * 128 * 4;       // 4 x [32 queries x 32 fp32]
-  static constexpr int kSlotBlock = 32 * 128;
+  static constexpr int kDS = kV + kPanels * kKvPanel;   // 128 keys x 64 queries BF16, MN-major
+  static constexpr int kUnits = D == 128 ? 2 : 1;       // staged units per step
+  static constexpr int kUnitRows = 64 / kUnits;
+  static constexpr int kSlots = 3;                      // staging ring of dQ units
+  static constexpr int kSlotBlock = kUnitRows * 128;    // [rows x 32 fp32]
+  static constexpr int kSlotBytes = (D / 32) * kSlotBlock;
   static constexpr int kStg = kDS + 128 * 128;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = D == 128 ? 3 : 6;
   static constexpr int kStage0 = kStg + kSlots * kSlotBytes;
-  static constexpr int kQ = 0, kDO = 2 * kQPanel;
-  static constexpr int kStageBytes = 4 * kQPanel;
+  static constexpr int kQ = 0, kDO = kPanels * kQPanel;
+  static constexpr int kStageBytes = 2 * kPanels * kQPanel;
   static constexpr int kLd = kStage0 + kStages * kStageBytes;   // per stage LSE2[64], Delta[64]
   static constexpr int kBars = kLd + kStages * 512;
   // kv; per stage full (Q, dO, LSE2, Delta) and empty (after the dK MMA);
@@ -78,7 +118,7 @@ struct BwdQ64Smem {
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;          // re-align the base to 1 KB
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int stage(int s) { return kStage0 + (s % kStages) * kStageBytes; }
   static constexpr int lse(int s) { return kLd + (s % kStages) * 512; }
   static constexpr int delta(int s) { return kLd + (s % kStages) * 512 + 256; }
@@ -110,27 +150,30 @@ __device__ __forceinline__ BwdWork bwd_q64_work(const BwdParams& p, int id) {
   return w;
 }
 
+template <int D>
 __device__ __forceinline__ int bwd_q64_work_id(uint32_t sbase) {
   int id;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(id) : "r"(sbase + BwdQ64Smem::kMisc + 8) : "memory");
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(id) : "r"(sbase + BwdQ64Smem<D>::kMisc + 8) : "memory");
   return id;
 }
 
 // ------------------------------------------------------------ load warp
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void bwd_q64_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                                   const CUtensorMap* tm_v, const CUtensorMap* tm_do,
                                                   uint32_t sbase, const BwdParams& p, const Waiter& w) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id(sbase));
+  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id<D>(sbase));
   if (wk.steps == 0) return;
-  mbar_arrive_expect_tx_warp(bar(L::bKv), 4u * L::kKvPanel);
+  mbar_arrive_expect_tx_warp(bar(L::bKv), (2u + L::kPanels) * L::kKvPanel);
 #pragma unroll
-  for (int pn = 0; pn < 2; ++pn) {
-    tma_load_4d_warp(sbase + L::kK + pn * L::kKvPanel, tm_k, bar(L::bKv), pn * 64, wk.g, wk.k0, wk.b);
+  for (int pn = 0; pn < 2; ++pn)
+    tma_load_4d_warp(sbase + L::kK + pn * L::kKvPanel, tm_k, bar(L::bKv), D == 128 ? pn * 64 : 0, wk.g, wk.k0,
+                     wk.b);
+#pragma unroll
+  for (int pn = 0; pn < L::kPanels; ++pn)
     tma_load_4d_warp(sbase + L::kV + pn * L::kKvPanel, tm_v, bar(L::bKv), pn * 64, wk.g, wk.k0, wk.b);
-  }
   const int per_head = wk.n_qb - wk.qb0;
   bool ok = true;
   int n = 0;   // stages issued
@@ -143,9 +186,9 @@ __device__ __forceinline__ void bwd_q64_load_role(const CUtensorMap* tm_q, const
         !(ok = w.wait_warp(bar(L::bEmpty + st), static_cast<uint32_t>(s / L::kStages - 1) & 1u,
                            L::bEmpty + st)))
       break;
-    mbar_arrive_expect_tx_warp(bar(L::bFull + st), 4u * L::kQPanel + 512u);
+    mbar_arrive_expect_tx_warp(bar(L::bFull + st), L::kStageBytes + 512u);
 #pragma unroll
-    for (int pn = 0; pn < 2; ++pn) {
+    for (int pn = 0; pn < L::kPanels; ++pn) {
       tma_load_4d_warp(stg + L::kDO + pn * L::kQPanel, tm_do, bar(L::bFull + st), pn * 64, h, qb * 64, wk.b);
       tma_load_4d_warp(stg + L::kQ + pn * L::kQPanel, tm_q, bar(L::bFull + st), pn * 64, h, qb * 64, wk.b);
     }
@@ -164,15 +207,15 @@ __device__ __forceinline__ void bwd_q64_load_role(const CUtensorMap* tm_q, const
 }
 
 // ------------------------------------------------------------ MMA warp
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void bwd_q64_mma_role(uint32_t sbase, uint32_t tmem, const BwdParams& p,
                                                  const Waiter& w) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id(sbase));
+  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id<D>(sbase));
   if (wk.steps == 0) return;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T
-  constexpr uint32_t kIdescTs = idesc_bf16_f32(128, 128, false, true);  // dV, dK
+  constexpr uint32_t kIdescTs = idesc_bf16_f32(128, D, false, true);    // dV, dK
   constexpr uint32_t kIdescDq = idesc_bf16_f32(128, 64, true, true);    // dQ^T: A, B MN-major
   constexpr uint32_t kHi = desc_hi_sw128(1024);
   const uint32_t k_lo = desc_lo_sw128(sbase + L::kK, 16), v_lo = desc_lo_sw128(sbase + L::kV, 16);
@@ -185,7 +228,7 @@ __device__ __forceinline__ void bwd_q64_mma_role(uint32_t sbase, uint32_t tmem, 
   auto issue_kq = [&](int s, uint32_t a_lo, int col, int opnd, int done) {
     const uint32_t b_lo = desc_lo_sw128(sbase + L::stage(s) + opnd, 16);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t a_off = ((kk >> 2) * L::kKvPanel + (kk & 3) * 32) >> 4;
       const uint32_t b_off = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
       mma_ss_lohi_warp(tmem + col + 64 * (s & 1), a_lo + a_off, kHi, b_lo + b_off, kHi, kIdescS,
@@ -281,16 +324,16 @@ __device__ __forceinline__ void bwd_q64_p(const uint32_t (&sv)[32], const float4
 // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
 // queries 32 (w / 4) .. + 31 of each step. At the end it writes half of the
 // columns of its rows of dK and dV.
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                                      const BwdParams& p, const Waiter& w) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3, ch = warp >> 2;
   const int r = wq * 32 + lane;                         // key row = dQ^T head-dim row = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id(sbase));
+  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id<D>(sbase));
   const int kabs = wk.k0 + r;
   const float c2 = p.scale_log2;
   const int shift = p.Sk - p.Sq;
@@ -366,16 +409,16 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
   }
   // ---- epilogue: this warp's half of dV and scale * dK -> BF16 -> global
   const int64_t orow = (static_cast<int64_t>(wk.b) * p.Sk + kabs) * p.Hkv + wk.g;
-  __nv_bfloat16* dv_row = p.dv + orow * 128 + ch * 64;
-  __nv_bfloat16* dk_row = p.dk + orow * 128 + ch * 64;
+  __nv_bfloat16* dv_row = p.dv + orow * D + ch * (D / 2);
+  __nv_bfloat16* dk_row = p.dk + orow * D + ch * (D / 2);
   if (ok && wk.steps > 0) {
     if (!w.wait(bar(L::bAcc), 0u, L::bAcc)) return;
     tc_fence_after_sync();
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < D / 64; ++c) {
       uint32_t x[32], y[32];
-      tmem_ld_x32(lane_base + L::kColDV + ch * 64 + 32 * c, x);
-      tmem_ld_x32(lane_base + L::kColDK + ch * 64 + 32 * c, y);
+      tmem_ld_x32(lane_base + L::kColDV + ch * (D / 2) + 32 * c, x);
+      tmem_ld_x32(lane_base + L::kColDK + ch * (D / 2) + 32 * c, y);
       tmem_wait_ld_x32(x);
       tmem_wait_ld_x32(y);
       if (row_live) {
@@ -398,7 +441,7 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
   } else if (ok && row_live) {
     // no query reads this key block: zero gradients
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < D / 16; ++i) {
       reinterpret_cast<uint4*>(dv_row)[i] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(dk_row)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -406,40 +449,48 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
 }
 
 // ------------------------------------------------------------ dQ^T read-out warps
-// Warp 12 + i reads TMEM lane quarter i of each step's dQ^T (head-dim rows
-// 32 i .. + 31, all 64 queries), frees the columns for the step after next,
-// and stages scale * dQ, one half of 32 queries at a time, in block i of a
-// ring slot (head-dim columns 32 i .. + 31, row = query): for each query the
-// warp's 32 lanes fill one 128-byte row.
+// Warp 12 + i reads TMEM lane quarter i of each step's dQ^T, frees the
+// columns for the step after next, and stages scale * dQ in a ring slot,
+// row = query, in the 32-column block of its head-dim rows: for each query
+// the warp's 32 lanes fill one 128-byte row.
+// Head dim 128: lanes = head-dim rows 32 i .. + 31, all 64 queries, staged in
+// two units of 32 queries. Head dim 64: lanes 64..127 repeat rows 0..63, so
+// warp i takes head-dim rows 32 (i % 2) .. + 31 of queries 32 (i / 2) .. + 31,
+// and the step is one unit.
+template <int D>
 __device__ __forceinline__ void bwd_q64_dq_role(uint32_t sbase, uint32_t tmem, int steps,
                                                 const BwdParams& p, const Waiter& w) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const uint32_t blk = sbase + L::kStg + wq * L::kSlotBlock + ((lane & 3) << 2);
+  constexpr int kCols = D == 128 ? 64 : 32;             // queries this warp reads per step
+  const int dblk = D == 128 ? wq : (wq & 1);            // 32-column block of dQ
+  const int q_first = D == 128 ? 0 : 32 * (wq >> 1);    // first query it reads
+  const uint32_t blk = sbase + L::kStg + dblk * L::kSlotBlock + ((lane & 3) << 2);
   for (int s = 0; s < steps; ++s) {
     if (!w.wait(bar(L::bDqFull), static_cast<uint32_t>(s) & 1u, L::bDqFull)) return;
     tc_fence_after_sync();
-    uint32_t x[64];
-    const uint32_t col = lane_base + L::kColDP + 64 * (s & 1);
-    tmem_ld_x32(col, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-    tmem_ld_x32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-    tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+    uint32_t x[kCols];
+    const uint32_t col = lane_base + L::kColDP + 64 * (s & 1) + q_first;
+#pragma unroll
+    for (int c = 0; c < kCols / 32; ++c) tmem_ld_x32(col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+#pragma unroll
+    for (int c = 0; c < kCols / 32; ++c) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
     tc_fence_before_sync();
     mbar_arrive(bar(L::bDqFree));
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int u = 2 * s + hh;                         // half-tile number
+    for (int hh = 0; hh < L::kUnits; ++hh) {
+      const int u = L::kUnits * s + hh;                 // staged unit number
       const int slot = u % L::kSlots;
       if (u >= L::kSlots &&
           !w.wait(bar(L::bSlotFree + slot), static_cast<uint32_t>(u / L::kSlots - 1) & 1u, L::bSlotFree + slot))
         return;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const uint32_t addr = blk + slot * L::kSlotBytes + j * 128 +
-                              (static_cast<uint32_t>((lane >> 2) ^ (j & 7)) << 4);
+        const int row = (D == 128 ? 0 : q_first) + j;   // query row within the unit
+        const uint32_t addr = blk + slot * L::kSlotBytes + row * 128 +
+                              (static_cast<uint32_t>((lane >> 2) ^ (row & 7)) << 4);
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(__uint_as_float(x[32 * hh + j]) * p.scale)
                      : "memory");
       }
@@ -450,25 +501,26 @@ __device__ __forceinline__ void bwd_q64_dq_role(uint32_t sbase, uint32_t tmem, i
 }
 
 // ------------------------------------------------------------ dQ flush warp
-// Adds each staged half-tile (32 queries x 128 columns) to the global fp32
-// accumulator with one bulk tensor reduce-add per 32 columns (rows past Sq
-// are outside the tensor and skipped). Up to two half-tiles are in flight: a
-// slot is handed back once the reduce-add issued after it has been issued
-// and its own source has been read. In deterministic mode the lane first
-// waits for its turn on the 64-query block's counter and, once both halves'
-// adds have completed, passes the turn on.
-template <bool CAUSAL>
+// Adds each staged unit (32 queries x 128 columns at head dim 128, 64 x 64
+// at 64) to the global fp32 accumulator with one bulk tensor reduce-add per
+// 32 columns (rows past Sq are outside the tensor and skipped). Up to two
+// units are in flight: a slot is handed back once the reduce-add issued
+// after it has been issued and its own source has been read. In
+// deterministic mode the lane first waits for its turn on the 64-query
+// block's counter and, once the step's last unit has completed, passes the
+// turn on.
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void bwd_q64_flush_role(const CUtensorMap* tm_dq, uint32_t sbase,
                                                    const BwdParams& p, const Waiter& w) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id(sbase));
+  const BwdWork wk = bwd_q64_work<CAUSAL>(p, bwd_q64_work_id<D>(sbase));
   const int per_head = wk.n_qb - wk.qb0;
   const int lane = threadIdx.x & 31;
   const int kb = wk.k0 / 128;
   bool ok = true;
-  for (int u = 0; u < 2 * wk.steps; ++u) {
-    const int s = u >> 1, hh = u & 1;
+  for (int u = 0; u < L::kUnits * wk.steps; ++u) {
+    const int s = u / L::kUnits, hh = u % L::kUnits;
     const int h = wk.g * p.group + s / per_head;
     const int qb = wk.qb0 + s % per_head;
     const int slot = u % L::kSlots;
@@ -501,11 +553,11 @@ __device__ __forceinline__ void bwd_q64_flush_role(const CUtensorMap* tm_dq, uin
       }
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < D / 32; ++c)
           tma_reduce_add_4d(tm_dq, sbase + L::kStg + slot * L::kSlotBytes + c * L::kSlotBlock, 32 * c, h,
-                            qb * 64 + 32 * hh, wk.b);
+                            qb * 64 + L::kUnitRows * hh, wk.b);
         bulk_commit_group();
-        if (turn && hh == 1) {
+        if (turn && hh == L::kUnits - 1) {
           bulk_wait_group0();                         // both halves' adds are done in global memory
           asm volatile("fence.proxy.async.global;" ::: "memory");
           __threadfence();
@@ -524,12 +576,12 @@ __device__ __forceinline__ void bwd_q64_flush_role(const CUtensorMap* tm_dq, uin
 }
 
 // ------------------------------------------------------------ kernel
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdQ64Threads, 1)
     fa4_bwd_q64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-  using L = BwdQ64Smem;
+  using L = BwdQ64Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -587,23 +639,23 @@ __global__ void __launch_bounds__(kBwdQ64Threads, 1)
   if (warp < 8) {
     regs_increase<kRegsCompute>();
     const Waiter w{abort_flag, p.status, kRoleSoftmax};
-    bwd_q64_compute_role<CAUSAL>(sbase, smem, tmem, p, w);
+    bwd_q64_compute_role<D, CAUSAL>(sbase, smem, tmem, p, w);
   } else if (warp < kBwdQ64WarpDq) {
     regs_decrease<kRegsIssue>();
     if (warp == kBwdWarpLoad) {
       const Waiter w{abort_flag, p.status, kRoleLoad};
-      bwd_q64_load_role<CAUSAL>(&tm_q, &tm_k, &tm_v, &tm_do, sbase, p, w);
+      bwd_q64_load_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, &tm_do, sbase, p, w);
     } else if (warp == kBwdWarpMma) {
       const Waiter w{abort_flag, p.status, kRoleMma};
-      bwd_q64_mma_role<CAUSAL>(sbase, tmem, p, w);
+      bwd_q64_mma_role<D, CAUSAL>(sbase, tmem, p, w);
     } else if (warp == kBwdWarpFlush) {
       const Waiter w{abort_flag, p.status, kRoleFlush};
-      bwd_q64_flush_role<CAUSAL>(&tm_dq, sbase, p, w);
+      bwd_q64_flush_role<D, CAUSAL>(&tm_dq, sbase, p, w);
     }
   } else {
     regs_decrease<kRegsDq>();
     const Waiter w{abort_flag, p.status, kRoleDqRead};
-    bwd_q64_dq_role(sbase, tmem, bwd_q64_work<CAUSAL>(p, bwd_q64_work_id(sbase)).steps, p, w);
+    bwd_q64_dq_role<D>(sbase, tmem, bwd_q64_work<CAUSAL>(p, bwd_q64_work_id<D>(sbase)).steps, p, w);
   }
 
   tc_fence_before_sync();

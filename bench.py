@@ -78,7 +78,7 @@ KERNEL_SOURCES = {
     "fa4_fwd_kernel": ["fa4_fwd_kernel.cuh", "fa4_ptx.cuh", "fa4_exp2.cuh", "fa4_launch.cuh",
                        "fa4_internal.h", "fa4_api.cu", "fa4_fwd_d128.cu", "fa4_fwd_d64.cu",
                        "fa4_fwd_fp8.cu", "fa4_merge.cu"],
-    "fa4_bwd_kernel": ["fa4_bwd_kernel.cuh", "fa4_bwd_q64.cuh", "fa4_bwd.cu", "fa4_fwd_kernel.cuh", "fa4_ptx.cuh",
+    "fa4_bwd_kernel": ["fa4_bwd_q64.cuh", "fa4_bwd.cu", "fa4_fwd_kernel.cuh", "fa4_ptx.cuh",
                        "fa4_exp2.cuh", "fa4_internal.h", "fa4_api.cu"],
 }
 

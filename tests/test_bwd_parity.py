@@ -68,6 +68,9 @@ CASES = [
     (2, 4, 4, 190, 333, 128, False),    # ragged both ways, 3 query steps of 64
     (1, 2, 2, 64, 256, 128, True),      # one 64-query step per head
     (1, 8, 1, 96, 128, 128, False),     # group of 8: 16 steps through one key block
+    (2, 4, 2, 200, 300, 64, True),      # head dim 64: GQA, ragged, bottom-right causal
+    (1, 8, 1, 96, 128, 64, False),      # head dim 64: 16 steps through one key block
+    (1, 2, 2, 1024, 1024, 64, True),    # head dim 64: several blocks each way
 ]
 
 
