@@ -150,6 +150,17 @@ __device__ __forceinline__ BwdWork bwd_q64_work(const BwdParams& p, int id) {
   return w;
 }
 
+// Query block of step s (its head is wk.g * group + s / (n_qb - qb0)). In
+// deterministic mode each head's blocks are walked from the last one down:
+// every key block then reaches a query block right after the key block
+// before it (in whose order the adds must come), instead of two blocks
+// ahead of it as an upward walk from each key block's diagonal would put it.
+__device__ __forceinline__ int bwd_q64_qb(const BwdWork& wk, const BwdParams& p, int s) {
+  const int per_head = wk.n_qb - wk.qb0;
+  const int r = s % per_head;
+  return p.dq_turn ? wk.n_qb - 1 - r : wk.qb0 + r;
+}
+
 template <int D>
 __device__ __forceinline__ int bwd_q64_work_id(uint32_t sbase) {
   int id;
@@ -179,7 +190,7 @@ __device__ __forceinline__ void bwd_q64_load_role(const CUtensorMap* tm_q, const
   int n = 0;   // stages issued
   for (int s = 0; s < wk.steps; ++s) {
     const int h = wk.g * p.group + s / per_head;
-    const int qb = wk.qb0 + s % per_head;
+    const int qb = bwd_q64_qb(wk, p, s);
     const int st = s % L::kStages;
     const uint32_t stg = sbase + L::stage(s);
     if (s >= L::kStages &&
@@ -344,7 +355,7 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
   for (int s = 0; s < wk.steps; ++s) {
     const int b = s & 1;
     const int st = s % L::kStages;
-    const int q0 = (wk.qb0 + s % per_head) * 64;
+    const int q0 = bwd_q64_qb(wk, p, s) * 64;
     const float4* lse4 = reinterpret_cast<const float4*>(smem + L::lse(s)) + 8 * ch;
     const float4* delta4 = reinterpret_cast<const float4*>(smem + L::delta(s)) + 8 * ch;
     if (!(ok = w.wait(bar(L::bFull + st), static_cast<uint32_t>(s / L::kStages) & 1u, L::bFull + st)))
@@ -522,7 +533,7 @@ __device__ __forceinline__ void bwd_q64_flush_role(const CUtensorMap* tm_dq, uin
   for (int u = 0; u < L::kUnits * wk.steps; ++u) {
     const int s = u / L::kUnits, hh = u % L::kUnits;
     const int h = wk.g * p.group + s / per_head;
-    const int qb = wk.qb0 + s % per_head;
+    const int qb = bwd_q64_qb(wk, p, s);
     const int slot = u % L::kSlots;
     if (!(ok = w.wait(bar(L::bSlotFull + slot), static_cast<uint32_t>(u / L::kSlots) & 1u, L::bSlotFull + slot)))
       break;
