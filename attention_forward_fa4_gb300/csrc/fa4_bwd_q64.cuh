@@ -127,16 +127,24 @@ struct BwdQ64Smem {
 template <bool CAUSAL>
 __device__ __forceinline__ BwdWork bwd_q64_work(const BwdParams& p, int id) {
   BwdWork w;
-  // Causal (and deterministic mode): key block outermost, so the longest
-  // CTAs (the first key blocks see the most queries) start first and the
-  // grid ends on short ones; in deterministic mode this also means every
-  // CTA whose turn comes earlier is already running. Otherwise the key
-  // blocks of one (batch, kv head) sit side by side (their CTAs share Q and
-  // dO in L2).
+  // Key blocks in groups of G, the groups in key order and every (batch, kv
+  // head) inside each group:
+  // - causal, G = 16: the longest CTAs (the first key blocks see the most
+  //   queries) start first and the grid ends on short ones, while the live
+  //   CTAs span few enough heads for their Q, dO and dQ accumulator to stay
+  //   in L2 (measured: 2.4x less DRAM traffic than G = 1, and faster);
+  // - deterministic mode, G = 1 (key block outermost: measured fastest for
+  //   its turn chain); a lower key block of a head always has a lower work
+  //   number, so every CTA whose turn comes earlier is already running;
+  // - otherwise G = n_kblk: the key blocks of one (batch, kv head) side by
+  //   side (their CTAs share Q and dO in L2).
   const int n_bg = p.B * p.Hkv;
-  const bool kb_major = CAUSAL || p.dq_turn;
-  const int kb = kb_major ? id / n_bg : id % p.n_kblk;
-  const int bg = kb_major ? id % n_bg : id / p.n_kblk;
+  const int G = p.dq_turn ? 1 : (CAUSAL ? 16 : p.n_kblk);
+  const int grp = id / (G * n_bg);
+  const int in_grp = min(G, p.n_kblk - grp * G);
+  const int rem = id - grp * G * n_bg;
+  const int bg = rem / in_grp;
+  const int kb = grp * G + rem % in_grp;
   w.b = bg / p.Hkv;
   w.g = bg - w.b * p.Hkv;
   w.k0 = kb * 128;
