@@ -123,7 +123,8 @@ def test_deterministic_mode_repeats_bit_for_bit_and_matches_oracle(case):
         _check(name, got, ref[name], log)
 
 
-@pytest.mark.parametrize("w", [workloads.MID, workloads.LONG_CAUSAL], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [workloads.MID, workloads.LONG_CAUSAL,
+                               workloads.by_name("d64_causal_b8_h32_s4096")], ids=lambda w: w.name)
 def test_bwd_full_size_sampled_heads(w):
     """The backward of a full-size workload in the launch the benchmark times
     (its seeded dO included); the gradients of the first and the last
