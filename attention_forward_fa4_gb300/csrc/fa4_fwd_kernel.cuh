@@ -81,7 +81,7 @@ constexpr uint32_t kTmemCols = 512;
 // A wait gives up after this many SM cycles (about 0.5 s at 2 GHz).
 constexpr long long kWaitLimitCycles = 1ll << 30;
 
-enum : unsigned { kStatusTimeout = 5u, kStatusMisalignedSmem = 3u };
+enum : unsigned { kStatusTimeout = 5u };
 enum : unsigned { kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleCorrection = 3, kRoleFlush = 4, kRoleDqRead = 5 };
 
 struct FwdParams {

@@ -332,14 +332,12 @@ fa4_status fa4_fwd_splitkv_static(const void *q, const void *k, const void *v, v
 
 /*
  * fa4_device_status -- synchronise the current device and return the
- * kernel-side status word: FA4_OK; FA4_ERR_TIMEOUT if any kernel of
- * this library gave up on a pipeline wait since the last clear; or
- * FA4_ERR_MISALIGNED if a backward kernel found its dynamic shared memory
- * not 1 KB aligned (it then exits without work). `detail`
+ * kernel-side status word: FA4_OK, or FA4_ERR_TIMEOUT if any kernel of
+ * this library gave up on a pipeline wait since the last clear. `detail`
  * (may be NULL) receives 4 words: the error code, the waiting role
  * (0 load, 1 mma, 2 softmax -- the backward's compute warps --,
- * 3 correction, 4 the backward's dQ flush warp, 5 the head-dim-128
- * backward's dQ^T read-out warps), the barrier id (an index
+ * 3 correction, 4 the backward's dQ flush warp, 5 the backward's dQ^T
+ * read-out warps), the barrier id (an index
  * into the kernel's own barrier table) and the block index. When `clear`
  * is non-zero the word is reset to FA4_OK.
  * Returns FA4_ERR_CUDA if the device cannot be reached.
