@@ -52,6 +52,11 @@ class _Options(ctypes.Structure):
                 ("test_stall_cycles", ctypes.c_longlong)]
 
 
+class _BwdOptions(ctypes.Structure):
+    """fa4_bwd_options (include/fa4.h)."""
+    _fields_ = [("deterministic", ctypes.c_int), ("test_stall_cycles", ctypes.c_longlong)]
+
+
 TRACE_EVENTS = 21
 TRACE_STEPS = 128
 TRACE_EVENT_NAMES = ("mma_s_wait", "mma_s_issued", "mma_pv_wait", "mma_pv_issued",
@@ -103,6 +108,11 @@ def load_library():
     lib.fa4_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
                                i32, i32, vp, ctypes.c_uint64, vp]
     lib.fa4_bwd_ex.restype = i32
+    lib.fa4_bwd_default_options.argtypes = [ctypes.POINTER(_BwdOptions)]
+    lib.fa4_bwd_default_options.restype = None
+    lib.fa4_bwd_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                                i32, ctypes.POINTER(_BwdOptions), vp, ctypes.c_uint64, vp]
+    lib.fa4_bwd_opt.restype = i32
     lib.fa4_fwd_default_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa4_fwd_default_options.restype = None
     lib.fa4_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint * 4)]
@@ -249,11 +259,13 @@ def bwd_workspace_bytes(B: int, Hq: int, Sq: int, d: int) -> int:
 def bwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              dout: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
              dv: torch.Tensor, causal: bool = False, scale: Optional[float] = None, *,
-             deterministic: bool = False, workspace: Optional[torch.Tensor] = None,
+             deterministic: bool = False, test_stall_cycles: int = 0,
+             workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> None:
-    """``fa4_bwd``: write dq, dk, dv (preallocated, BF16) for the upstream
+    """``fa4_bwd_opt``: write dq, dk, dv (preallocated, BF16) for the upstream
     gradient ``dout``; ``o`` and ``lse`` are the forward's outputs.
-    ``workspace`` (CUDA uint8) is allocated here when omitted."""
+    ``workspace`` (CUDA uint8) is allocated here when omitted.
+    ``test_stall_cycles`` > 0 is a diagnostic that makes the launch time out."""
     lib = load_library()
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
@@ -275,11 +287,15 @@ def bwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
-    code = lib.fa4_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv,
-                          Sq, Sk, d, float(scale), int(bool(causal)), int(bool(deterministic)),
-                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
-    _check(code, "fa4_bwd_ex")
+    opt = _BwdOptions()
+    lib.fa4_bwd_default_options(ctypes.byref(opt))
+    opt.deterministic = int(bool(deterministic))
+    opt.test_stall_cycles = int(test_stall_cycles)
+    code = lib.fa4_bwd_opt(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv,
+                           Sq, Sk, d, float(scale), int(bool(causal)), ctypes.byref(opt),
+                           workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(code, "fa4_bwd_opt")
 
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,

@@ -491,8 +491,30 @@ fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o
                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                       int Sq, int Sk, int d, float scale, int causal, int deterministic,
                       void* workspace, uint64_t workspace_bytes, fa4_stream_t stream) {
+  fa4_bwd_options op;
+  fa4_bwd_default_options(&op);
+  op.deterministic = deterministic;
+  return fa4_bwd_opt(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, scale, causal, &op,
+                     workspace, workspace_bytes, stream);
+}
+
+void fa4_bwd_default_options(fa4_bwd_options* opt) {
+  if (!opt) return;
+  opt->deterministic = 0;
+  opt->test_stall_cycles = 0;
+}
+
+fa4_status fa4_bwd_opt(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int Sq, int Sk, int d, float scale, int causal, const fa4_bwd_options* opt,
+                       void* workspace, uint64_t workspace_bytes, fa4_stream_t stream) {
   using namespace fa4;
+  fa4_bwd_options op;
+  fa4_bwd_default_options(&op);
+  if (opt) op = *opt;
+  const int deterministic = op.deterministic;
   if (deterministic != 0 && deterministic != 1) return FA4_ERR_INVALID_ARG;
+  if (op.test_stall_cycles < 0) return FA4_ERR_INVALID_ARG;
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return FA4_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA4_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA4_ERR_INVALID_ARG;
@@ -565,7 +587,7 @@ fa4_status fa4_bwd_ex(const void* q, const void* k, const void* v, const void* o
                                static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv), dq_acc, lse2, delta,
                                deterministic ? turns : nullptr, deterministic ? ticket : nullptr,
-                               B, Hq, Hkv, Sq, Sk, d, scale, causal != 0, status, s);
+                               B, Hq, Hkv, Sq, Sk, d, scale, causal != 0, op.test_stall_cycles, status, s);
   return err == cudaSuccess ? FA4_OK : FA4_ERR_CUDA;
 }
 

@@ -81,7 +81,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
                        float* dq_acc, float* lse2, float* delta, int* dq_turn, int* cta_ticket,
                        int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale, bool causal,
-                       unsigned int* status, cudaStream_t s) {
+                       long long test_stall_cycles, unsigned int* status, cudaStream_t s) {
   const int Sq_pad = (Sq + 127) / 128 * 128;
   const int64_t dq_elems = static_cast<int64_t>(B) * Sq * Hq * d;
   cudaError_t err = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(dq_elems) * 4, s);
@@ -117,6 +117,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.status = status;
   p.dq_turn = dq_turn;
   p.cta_ticket = cta_ticket;
+  p.test_stall_cycles = test_stall_cycles;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(p.n_kblk) * B * Hkv);
   if (d == 64)
     err = causal ? launch_q64<64, true>(tq, tk, tv, tdo, tdq, p, grid, s)

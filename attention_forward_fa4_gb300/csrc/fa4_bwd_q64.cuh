@@ -68,6 +68,9 @@ struct BwdParams {
   // number when it starts, so every lower number belongs to a CTA that is
   // already running whatever order the hardware dispatched them in.
   int* cta_ticket;
+  // Diagnostic (> 0): the compute warps first wait this many cycles on a
+  // barrier nothing completes, so the launch takes the timeout path.
+  long long test_stall_cycles;
 };
 
 // The CTA's key block and the query blocks it visits.
@@ -113,7 +116,8 @@ struct BwdQ64Smem {
   static constexpr int bKv = 0, bFull = 1, bEmpty = bFull + kStages, bS = bEmpty + kStages,
                        bDP = bS + 2, bPReady = bDP + 2, bDqFull = bPReady + 1, bDqFree = bDqFull + 1,
                        bAcc = bDqFree + 1, bSlotFull = bAcc + 1, bSlotFree = bSlotFull + kSlots,
-                       kNumBars = bSlotFree + kSlots;
+                       bStall = bSlotFree + kSlots,   // never completed (timeout test)
+                       kNumBars = bStall + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem base, abort flag, work number
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;          // re-align the base to 1 KB
@@ -360,7 +364,9 @@ __device__ __forceinline__ void bwd_q64_compute_role(uint32_t sbase, uint8_t* sm
   const bool row_live = kabs < p.Sk;
   const bool rows_live = wk.k0 + 128 <= p.Sk;          // every key row of the block exists
   bool ok = true;
-  for (int s = 0; s < wk.steps; ++s) {
+  if (p.test_stall_cycles > 0)   // diagnostic: a wait nothing ends
+    ok = w.wait_for(bar(L::bStall), 0u, L::bStall, p.test_stall_cycles);
+  for (int s = 0; ok && s < wk.steps; ++s) {
     const int b = s & 1;
     const int st = s % L::kStages;
     const int q0 = bwd_q64_qb(wk, p, s) * 64;
@@ -630,6 +636,7 @@ __global__ void __launch_bounds__(kBwdQ64Threads, 1)
     mbar_init(bar(L::bDqFull), 1);
     mbar_init(bar(L::bDqFree), 128);
     mbar_init(bar(L::bAcc), 1);
+    mbar_init(bar(L::bStall), 1);
     for (int i = 0; i < L::kSlots; ++i) {
       mbar_init(bar(L::bSlotFull + i), 128);
       mbar_init(bar(L::bSlotFree + i), 1);

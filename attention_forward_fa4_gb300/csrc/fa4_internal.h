@@ -43,14 +43,14 @@ FA4_DECLARE_LAUNCH(launch_fwd_d128_traced)
 #undef FA4_DECLARE_LAUNCH
 
 // Attention backward (fa4_bwd.cu): zero dq_acc, preprocess (lse2, delta),
-// main kernel (dK, dV, atomic dQ), dq_acc -> dq.
+// main kernel (dK, dV, dQ reduce-adds), dq_acc -> dq.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const __nv_bfloat16* o,
                        const __nv_bfloat16* dout,
                        const float* lse, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
                        float* dq_acc, float* lse2, float* delta, int* dq_turn, int* cta_ticket,
                        int B, int Hq, int Hkv, int Sq, int Sk, int d, float scale, bool causal,
-                       unsigned int* status, cudaStream_t s);
+                       long long test_stall_cycles, unsigned int* status, cudaStream_t s);
 
 // FP8 forward (e4m3 Q, K, V; head dim 128).
 cudaError_t launch_fwd_d128_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -258,6 +258,32 @@ fa4_status fa4_bwd_ex(const void *q, const void *k, const void *v, const void *o
                       int deterministic, void *workspace, uint64_t workspace_bytes,
                       fa4_stream_t stream);
 
+/* Options of fa4_bwd_opt. Fill with fa4_bwd_default_options() first. */
+typedef struct fa4_bwd_options {
+    /* 0 or 1, as fa4_bwd_ex's deterministic. */
+    int deterministic;
+    /* Diagnostic, >= 0; 0 (the default) disables it. With a positive value
+     * the compute warps first wait on a barrier that nothing completes, for
+     * that many SM cycles: the wait runs out and the launch takes the
+     * timeout path (fa4_device_status reports FA4_ERR_TIMEOUT with role 2;
+     * dk and dv are not written). Tests use it; results are meaningless. */
+    long long test_stall_cycles;
+} fa4_bwd_options;
+
+/* Default options: deterministic = 0, test_stall_cycles = 0. */
+void fa4_bwd_default_options(fa4_bwd_options *opt);
+
+/*
+ * fa4_bwd_opt -- fa4_bwd with options (NULL: the defaults). Arguments,
+ * workspace and return codes as fa4_bwd; FA4_ERR_INVALID_ARG also for
+ * deterministic outside {0, 1} or a negative test_stall_cycles.
+ */
+fa4_status fa4_bwd_opt(const void *q, const void *k, const void *v, const void *o,
+                       const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                       int Hq, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                       const fa4_bwd_options *opt, void *workspace, uint64_t workspace_bytes,
+                       fa4_stream_t stream);
+
 /*
  * fa4_fwd_splitkv -- the same forward, with the keys cut into num_splits
  * contiguous ranges of whole 128-key blocks that separate CTAs process in

@@ -148,3 +148,22 @@ def test_fp8_and_host_entry_points_check_arguments_first(lib):
     assert host(q=0) == fa4.FA4_ERR_INVALID_ARG
     assert host(scale=-1.0) == fa4.FA4_ERR_INVALID_ARG
     assert host(B=0) == fa4.FA4_OK        # empty: nothing to copy or compute
+
+
+def test_bwd_options_are_checked_before_cuda(lib):
+    """fa4_bwd_opt rejects a deterministic flag outside {0, 1} and a negative
+    diagnostic stall before any device call; the defaults are off."""
+    import attention_forward_fa4_gb300 as fa4
+    opt = fa4._BwdOptions()
+    lib.fa4_bwd_default_options(ctypes.byref(opt))
+    assert opt.deterministic == 0 and opt.test_stall_cycles == 0
+    P = 1 << 20       # 16-byte aligned fake device addresses: never dereferenced here
+
+    def call(o):
+        return lib.fa4_bwd_opt(P, P + 4096, P + 8192, P + 12288, P + 16384, P + 20480, P + 24576,
+                               P + 28672, P + 32768, 1, 2, 2, 64, 64, 64, 0.125, 0,
+                               ctypes.byref(o), P + 65536, 1 << 20, None)
+    bad = fa4._BwdOptions(deterministic=2, test_stall_cycles=0)
+    assert call(bad) == fa4.FA4_ERR_INVALID_ARG
+    bad = fa4._BwdOptions(deterministic=0, test_stall_cycles=-1)
+    assert call(bad) == fa4.FA4_ERR_INVALID_ARG
