@@ -23,7 +23,9 @@
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_t  = Q_t K_j^T   fp32, columns [128 t, 128 t + 128)
-//   P_t  (BF16, two per column) aliases the first 64 columns of S_t
+//   P_t  (BF16, two per column) aliases the first 64 columns of S_t; in
+//        the persistent grid at head dim 64 it has its own columns
+//        [384 + 64 t, 448 + 64 t) instead (see OwnP)
 //   O_t  fp32, columns [256 + D t, 256 + D t + D)
 //
 // The MMA thread issues the two tiles' work in ping-pong order (see
@@ -197,7 +199,8 @@ struct Smem {
   static constexpr int bOFree = bQEmpty + 1;             // [2] epilogue has read O_t
   static constexpr int bDrain = bOFree + 2;
   static constexpr int bStall = bDrain + 1;              // never completed (timeout test)
-  static constexpr int kNumBars = bStall + 1;
+  static constexpr int bSFree = bStall + 1;              // [2] softmax has read S_t (own-P layout)
+  static constexpr int kNumBars = bSFree + 2;
   // Rescale hand-off from softmax to correction, double-buffered by step
   // parity: alpha float [2 buffers][2 tiles][128], flags int [2][2][4].
   static constexpr int kAlpha = kBars + kNumBars * 8;
@@ -208,6 +211,27 @@ struct Smem {
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  // At head dim 64 the two O tiles leave 128 columns free, so P_t can have
+  // its own 64 columns instead of aliasing S_t ("own P", see OwnP below).
+  static constexpr bool kPColsFree = (D == 64 && !FP8);
+  static constexpr uint32_t kColP0 = 256 + 2 * D, kColP1 = 256 + 2 * D + 64;
+  static_assert(!kPColsFree || kColP1 + 64 <= 512, "P columns beyond tensor memory");
+};
+
+// Own P: P_t in its own tensor-memory columns. The next S_t MMA then only
+// waits until the softmax has read S_t into registers, not for the P*V that
+// reads P_t, so S_t(j+1) is computed while softmax_t(j) runs; every P*V
+// commits pv_done, which the softmax waits for before it overwrites P_t or
+// rescales O_t. Used by the persistent grid at head dim 64 (short
+// sequences), where it measured faster; with one CTA per work tile the
+// MMA warp's extra waits and commits cost more than the overlap gains.
+template <int D, bool PERSIST, bool FP8>
+struct OwnP {
+  static constexpr bool value = Smem<D, FP8>::kPColsFree && PERSIST;
+  static constexpr uint32_t col(int t) {
+    return value ? (t == 0 ? Smem<D, FP8>::kColP0 : Smem<D, FP8>::kColP1)
+                 : (t == 0 ? Smem<D, FP8>::kColS0 : Smem<D, FP8>::kColS1);
+  }
 };
 
 // ------------------------------------------------------------ bounded waits
@@ -413,6 +437,10 @@ __device__ __forceinline__ void load_role(const CUtensorMap* tm_q, const CUtenso
 // otherwise idle); the whole warp computing the same uniform operands and
 // one elected lane issuing brought it to about 850.
 //
+// With own P (OwnP) the order per key block is S_0(j+1), S_1(j+1), then
+// O_0 += P_0(j) V_j, O_1 += P_1(j) V_j: the S MMAs only wait until the
+// softmax has read S_t(j), and strict order changes nothing.
+//
 // Phases run on across the CTA's work tiles: the ring position, the count
 // of P*V MMAs per query tile and the count of earlier tiles whose O_t the
 // epilogue has to read before the next tile's first P*V overwrites it.
@@ -426,6 +454,8 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
   constexpr uint32_t kHi = desc_hi_sw128(1024);                          // 8 rows x 128 B
   const uint32_t col_s[2] = {L::kColS0, L::kColS1};
   const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+  constexpr bool kOwnP = OwnP<D, PERSIST, FP8>::value;
+  const uint32_t col_p[2] = {OwnP<D, PERSIST, FP8>::col(0), OwnP<D, PERSIST, FP8>::col(1)};
 #ifdef FA4_PROF
   unsigned pm_acc[4] = {0, 0, 0, 0}, pm_n = 0, pm_pw = 0;
 #endif
@@ -475,14 +505,14 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
         constexpr uint32_t kIdescPv8 = idesc_e4m3_f32(kBM, D, false, true);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
-          mma_ts_lohi_f8_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (4096 >> 4), kHi,
+          mma_ts_lohi_f8_warp(tmem + col_o[t], tmem + col_p[t] + kk * 8, v_lo + kk * (4096 >> 4), kHi,
                               kIdescPv8, (!first || kk > 0) ? 1u : 0u);
       } else {
 #pragma unroll
         for (int k = 0; k < kBN / 16 / FA4_P_SLICES; ++k) {
           // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2 KB) of V.
           const int kk = half * (kBN / 16 / FA4_P_SLICES) + k;
-          mma_ts_lohi_warp(tmem + col_o[t], tmem + col_s[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
+          mma_ts_lohi_warp(tmem + col_o[t], tmem + col_p[t] + kk * 8, v_lo + kk * (2048 >> 4), kHi,
                       kIdescPV, (!first || kk > 0) ? 1u : 0u);
         }
       }
@@ -503,6 +533,7 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 
   int cons = 0;                 // ring positions consumed
   int n_q = 0;                  // Q tile pairs consumed
+  int n_s[2] = {0, 0};          // S MMAs issued per query tile
   int n_pv[2] = {0, 0};         // P*V MMAs issued per query tile
   int n_epi[2] = {0, 0};        // earlier work tiles whose O_t the epilogue reads
   bool ok = true;
@@ -518,13 +549,79 @@ __device__ __forceinline__ void mma_role(uint32_t sbase, uint32_t tmem, const Fw
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (tl.nkv[t] == 0) continue;
+      if constexpr (kOwnP) {
+        // the softmax must have read the previous work tile's last S_t
+        if (n_s[t] > 0 &&
+            !(ok = w.wait_warp(bar(L::bSFree + t), static_cast<uint32_t>(n_s[t] - 1) & 1u, L::bSFree + t)))
+          break;
+        tc_fence_after_sync();
+        ++n_s[t];
+      }
       trace_mark_lane0<TRACE>(p, kTrMmaSGo, 0, t, iter);
       issue_s(t, cons % L::kSlots);
       trace_mark_lane0<TRACE>(p, kTrMmaSIssued, 0, t, iter);
     }
+    if (kOwnP && !ok) break;
     mma_commit_warp(bar(L::bKvEmpty + cons % L::kSlots));
     ++cons;
     if (tl.nkv_max == 1) mma_commit_warp(bar(L::bQEmpty));     // no further S of this tile
+    if constexpr (kOwnP) {
+      // P_t has its own columns: per key block j, first S_t(j+1) for both
+      // tiles (each as soon as softmax_t(j) has read S_t(j)), then
+      // O_t += P_t(j) V_j for both tiles, each followed by a pv_done commit.
+      for (int j = 0; ok && j < tl.nkv_max; ++j) {
+        const int vpos = cons, kpos = cons + 1;             // V_j, then K_{j+1}
+        const bool next = j + 1 < tl.nkv_max;
+        if (next) {
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j + 1 >= tl.nkv[t]) continue;
+            trace_mark_lane0<TRACE>(p, kTrMmaSWait, j + 1, t, iter);
+            if (!(ok = w.wait_warp(bar(L::bSFree + t), static_cast<uint32_t>(n_s[t] - 1) & 1u,
+                                   L::bSFree + t)))
+              break;
+            tc_fence_after_sync();
+            if (!k_ready) {
+              if (!(ok = wait_slot(kpos))) break;
+              k_ready = true;
+            }
+            trace_mark_lane0<TRACE>(p, kTrMmaSGo, j + 1, t, iter);
+            issue_s(t, kpos % L::kSlots);
+            ++n_s[t];
+            trace_mark_lane0<TRACE>(p, kTrMmaSIssued, j + 1, t, iter);
+          }
+          if (!ok) break;
+          // K_{j+1} was needed by at least one tile (the one with nkv_max blocks).
+          mma_commit_warp(bar(L::bKvEmpty + kpos % L::kSlots));
+          // The last S MMAs of this work tile are issued: once they complete
+          // the Q buffers may take the next tile's queries.
+          if (j + 2 == tl.nkv_max) mma_commit_warp(bar(L::bQEmpty));
+        }
+        if (!(ok = wait_slot(vpos))) break;
+        trace_mark_lane0<TRACE>(p, kTrMmaVReady, j, 0, iter);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j >= tl.nkv[t]) continue;
+          trace_mark_lane0<TRACE>(p, kTrMmaPvWait, j, t, iter);
+          if (p.correction_wg &&
+              !(ok = w.wait_warp(bar(L::bOReady + t), static_cast<uint32_t>(n_pv[t]) & 1u, L::bOReady + t)))
+            break;
+          if (j == 0 && n_epi[t] > 0 &&     // the previous tile's O_t must have been read out
+              !(ok = w.wait_warp(bar(L::bOFree + t), static_cast<uint32_t>(n_epi[t] - 1) & 1u, L::bOFree + t)))
+            break;
+          tc_fence_after_sync();
+          trace_mark_lane0<TRACE>(p, kTrMmaPvGo, j, t, iter);
+          if (!(ok = issue_pv(t, vpos % L::kSlots, j == 0, n_pv[t], true))) break;
+          ++n_pv[t];
+          trace_mark_lane0<TRACE>(p, kTrMmaPvIssued, j, t, iter);
+        }
+        if (!ok) break;
+        mma_commit_warp(bar(L::bKvEmpty + vpos % L::kSlots));
+        cons += next ? 2 : 1;
+        trace_mark_lane0<TRACE>(p, kTrMmaCommitted, j, 0, iter);
+      }
+    } else
     for (int j = 0; ok && j < tl.nkv_max; ++j) {
       const int vpos = cons, kpos = cons + 1;             // V_j, then K_{j+1}
       const bool next = j + 1 < tl.nkv_max;
@@ -644,7 +741,11 @@ __device__ __forceinline__ void correction_role(uint32_t sbase, uint8_t* smem, u
           // This 32-row group's reference max moved: O_t <- alpha * O_t, then
           // release the group. The previous P*V into O_t has completed: the
           // S MMA issued behind it had completed before the softmax warps
-          // arrived on p_full.
+          // arrived on p_full. With its own P columns no S MMA is issued
+          // behind it, so wait for its pv_done commit.
+          if (OwnP<D, PERSIST, FP8>::value &&
+              !w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(cnt - 1) & 1u, L::bPvDone + t))
+            return;
           tc_fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
@@ -721,6 +822,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   volatile int* flags_s = reinterpret_cast<volatile int*>(smem + L::kFlags);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t s_addr = lane_base + (t == 0 ? L::kColS0 : L::kColS1);
+  constexpr bool kOwnP = OwnP<D, PERSIST, FP8>::value;
+  const uint32_t p_addr = lane_base + OwnP<D, PERSIST, FP8>::col(t);
   const uint32_t o_addr = lane_base + (t == 0 ? L::kColO0 : L::kColO1);
   const float cl2 = p.scale_log2;
   const int shift = p.Sk - p.Sq;
@@ -763,6 +866,25 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[64]));
     tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    // With its own P columns, the MMA warp may compute the next S_t into
+    // these columns as soon as all four warps have read them.
+    if constexpr (kOwnP) {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bSFree + t));
+    }
+    // Own P: before this step rescales O_t or overwrites P_t, the previous
+    // step's P*V must have completed (the S MMA this step waited for was
+    // issued before it, so its commit does not track it). At j = 0 the
+    // epilogue of the previous work tile has waited for its last P*V.
+    bool pv_prev_done = !kOwnP || j == 0;
+    auto wait_pv_prev = [&]() -> bool {
+      if (pv_prev_done) return true;
+      pv_prev_done = true;
+      const bool r = w.wait(bar(L::bPvDone + t), static_cast<uint32_t>(n_step - 1) & 1u, L::bPvDone + t);
+      tc_fence_after_sync();
+      return r;
+    };
     FA4_PROF_CLK(pr_t1);
     if (tracer) trace_mark<TRACE>(p, kTrSmLoaded, j, t, iter);
     const int kb = tl.kv0 + j;           // absolute key block
@@ -799,8 +921,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
             ++n_rescaled;
             // O_t <- alpha * O_t for this warp's rows. The previous P*V into
             // O_t has completed: the S MMA issued behind it, whose commit this
-            // step waited for, tracks it too.
-
+            // step waited for, tracks it too (with its own P columns, the
+            // explicit pv_done wait).
+            if constexpr (kOwnP) {
+              if (!wait_pv_prev()) ok = false;
+            }
 #pragma unroll 1
             for (int c = 0; c < D / 16; ++c) {
               uint32_t x[16];
@@ -821,6 +946,22 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
         pr_t2 = static_cast<unsigned>(clock());
 #endif
         return;
+      }
+      // Own P: S_t(j+1) is issued before P_t(j) V_j, so this step may run a
+      // whole step ahead of the consumers of p_full and o_ready. Before it
+      // arrives on either, the correction warps must have taken the previous
+      // step's hand-off (which also frees the buffer this step reuses, two
+      // steps on) and the MMA warp its o_ready (its P*V has completed);
+      // otherwise a phase could complete twice before its consumer looks.
+      // Without own P the next S follows the P*V that waits for o_ready, and
+      // the hand-off check stays at the end of the step (below), off the
+      // step's path.
+      if constexpr (kOwnP) {
+        if (n_step >= 1 &&
+            !w.wait(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
+                    L::bCDone + 2 * t + (buf ^ 1)))
+          ok = false;
+        if (!wait_pv_prev()) ok = false;
       }
       if (warp_need) {
         const float alpha = (m_cand == -INFINITY) ? 1.0f : ex2_mufu(m_ref - m_cand);
@@ -859,8 +1000,14 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     }
     FA4_PROF_CLK(pr_t3);
     if (tracer) trace_mark<TRACE>(p, kTrSmExpDone, j, t, iter);
-    // P goes to the first kPCols columns of S_t, released to the P*V MMAs
-    // in kSlices parts (the FP8 forward always releases it whole)
+    // Own P: the previous P*V must have read P_t before it is overwritten.
+    if constexpr (kOwnP) {
+      if (!wait_pv_prev()) ok = false;
+      if (!ok) break;
+    }
+    // P goes to the first kPCols columns of S_t (at head dim 64 to its own
+    // columns), released to the P*V MMAs in kSlices parts (the FP8 forward
+    // always releases it whole)
     constexpr int kPCols = FP8 ? 32 : 64;
     constexpr int kSlices = FP8 ? 1 : FA4_P_SLICES;
     constexpr int kSliceCols = kPCols / kSlices;
@@ -868,7 +1015,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     for (int half = 0; half < kSlices; ++half) {
 #pragma unroll
       for (int q = 0; q < kSliceCols / 32; ++q)
-        tmem_st_x32(s_addr + half * kSliceCols + q * 32,
+        tmem_st_x32(p_addr + half * kSliceCols + q * 32,
                     *reinterpret_cast<const uint32_t(*)[32]>(&pk[half * kSliceCols + q * 32]));
       tmem_wait_st();
       tc_fence_before_sync();
@@ -895,7 +1042,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
     // The next step reuses the buffer of step n_step - 1: the correction
     // warps must have read it. Checked here, where the warp would otherwise
     // only wait for the next S, rather than on the next step's path.
-    if (p.correction_wg && n_step >= 1 &&
+    if (!kOwnP && p.correction_wg && n_step >= 1 &&
         !(ok = w.wait(bar(L::bCDone + 2 * t + (buf ^ 1)), static_cast<uint32_t>((n_step - 1) >> 1) & 1u,
                       L::bCDone + 2 * t + (buf ^ 1))))
       break;
@@ -915,9 +1062,10 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t sbase, uint8_t* sme
   __nv_bfloat16* orow = p.o + orow_idx * static_cast<int64_t>(D);
   float* prow = p.o_part + (part_off + orow_idx) * static_cast<int64_t>(D);
   if (n > 0) {
-    // one pv_done commit per work tile (per step in strict order)
-    const uint32_t pv_par = p.strict_order ? static_cast<uint32_t>(n_step - 1) & 1u
-                                           : static_cast<uint32_t>(n_fin) & 1u;
+    // one pv_done commit per work tile (per step in strict order and with
+    // own P)
+    const uint32_t pv_par = (p.strict_order || kOwnP) ? static_cast<uint32_t>(n_step - 1) & 1u
+                                                      : static_cast<uint32_t>(n_fin) & 1u;
     ++n_fin;
     if (!(ok = w.wait(bar(L::bPvDone + t), pv_par, L::bPvDone + t)))
       break;
@@ -1019,6 +1167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::bQEmpty), 1);
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bStall), 1);
+    mbar_init(bar(L::bSFree), 4);
+    mbar_init(bar(L::bSFree + 1), 4);
     for (int i = 0; i < 16; ++i) reinterpret_cast<volatile int*>(smem + L::kFlags)[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();

@@ -93,7 +93,10 @@ typedef struct {
      * relying on the tensor core running one thread's MMAs in issue order
      * (the two-tile ping-pong of "FlashAttention-4" §3.1.2). 1: wait for
      * the P_t*V MMA to complete first (slower; the PTX memory model only
-     * promises issue order for MMAs into the same accumulator). */
+     * promises issue order for MMAs into the same accumulator). At head
+     * dimension 64 in the persistent grid (grid_mode 2, or chosen
+     * automatically) P_t has its own tensor-memory columns, no score MMA
+     * overwrites it, and the flag changes nothing. */
     int strict_mma_order;
     /* Grid of CTAs: 0 (default) chooses automatically; 1: one CTA per work
      * tile (two 128-row query tiles of one batch and head), scheduled by the

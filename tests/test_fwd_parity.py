@@ -232,3 +232,41 @@ def test_grid_modes_agree_bit_for_bit(shape):
     o1, l1 = _run(q, k, v, causal, grid_mode=1)
     o2, l2 = _run(q, k, v, causal, grid_mode=2)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------ own P columns
+# At head dim 64 the persistent grid keeps P_t in its own tensor-memory
+# columns and computes S_t(j+1) while softmax_t(j) runs. The shapes give
+# more work tiles than SMs, so CTAs run several tiles back to back (the
+# hand-offs of S, P and O across tiles), with ragged tails, GQA and wide
+# logits (frequent rescales).
+OWN_P_SHAPES = [
+    # B, Hq, Hkv, Sq, Sk, d, causal
+    (2, 40, 8, 300, 700, 64, True),
+    (2, 40, 8, 300, 700, 64, False),
+    (1, 80, 80, 520, 260, 64, True),
+]
+
+
+@pytest.mark.parametrize("cwg", [False, True], ids=["inline", "corr_wg"])
+@pytest.mark.parametrize("shape", OWN_P_SHAPES, ids=lambda c: "x".join(map(str, c)))
+def test_own_p_persistent_matches_oracle(shape, cwg):
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=45, dist="wide")
+    _full_check(q, k, v, causal, 1.0 / math.sqrt(d), f"own P {shape}", grid_mode=2,
+                correction_warpgroup=cwg)
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0])
+@pytest.mark.parametrize("shape", [(4, 32, 8, 1024, 1024, 64, True), (8, 16, 16, 777, 1200, 64, False)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_own_p_equals_aliased_p_bit_for_bit(shape, tau):
+    """The persistent grid (own P columns, several tiles per CTA) and one CTA
+    per work tile (P aliasing S) compute the same products in the same
+    order: identical outputs, in both correction modes."""
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = workloads.make_custom(B, Hq, Hkv, Sq, Sk, d, seed=46, dist="wide")
+    o1, l1 = _run(q, k, v, causal, tau=tau, grid_mode=1)
+    for cwg in (False, True):
+        o2, l2 = _run(q, k, v, causal, tau=tau, grid_mode=2, correction_warpgroup=cwg)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
