@@ -77,13 +77,14 @@ unsigned int* status_ptr(int dev) {
 // short (few key blocks each), where per-CTA start-up is a large share of a
 // tile; long tiles keep one CTA per tile and the hardware's dynamic dispatch.
 // Measured on GB300 over head dims 64 / 128, 512 to 32768 keys: persistent
-// wins up to 8 key blocks at either head dim, and at head dim 64 up to 16
-// blocks (32 when causal, whose tiles are shorter on average); elsewhere
-// one CTA per tile is as fast or faster.
+// wins up to 8 key blocks at either head dim, and at head dim 64 (where its
+// kernel keeps P in its own tensor-memory columns) up to 32 blocks;
+// elsewhere one CTA per tile is as fast or faster.
 bool use_persistent_grid(int64_t n_tiles, int sms, int nblk, int d, bool causal) {
+  (void)causal;
   if (n_tiles <= sms) return false;
   if (nblk <= 8) return true;
-  return d == 64 && nblk <= (causal ? 32 : 16);
+  return d == 64 && nblk <= 32;
 }
 
 // Number of SMs of `dev` (looked up once each).
