@@ -133,17 +133,19 @@ __device__ __forceinline__ BwdWork bwd_q64_work(const BwdParams& p, int id) {
   BwdWork w;
   // Key blocks in groups of G, the groups in key order and every (batch, kv
   // head) inside each group:
-  // - causal, G = 16: the longest CTAs (the first key blocks see the most
+  // - causal, G = 24: the longest CTAs (the first key blocks see the most
   //   queries) start first and the grid ends on short ones, while the live
   //   CTAs span few enough heads for their Q, dO and dQ accumulator to stay
-  //   in L2 (measured: 2.4x less DRAM traffic than G = 1, and faster);
+  //   in L2. Measured on long causal (TFLOP/s, DRAM bytes per launch):
+  //   G = 1 1061 / 2.91 GB, 16 1068 / 1.23 GB, 24 1072 / 0.97 GB,
+  //   32 1056 / 0.83 GB, n_kblk (heads outermost) 1028 / 0.63 GB;
   // - deterministic mode, G = 1 (key block outermost: measured fastest for
   //   its turn chain); a lower key block of a head always has a lower work
   //   number, so every CTA whose turn comes earlier is already running;
   // - otherwise G = n_kblk: the key blocks of one (batch, kv head) side by
   //   side (their CTAs share Q and dO in L2).
   const int n_bg = p.B * p.Hkv;
-  const int G = p.dq_turn ? 1 : (CAUSAL ? 16 : p.n_kblk);
+  const int G = p.dq_turn ? 1 : (CAUSAL ? 24 : p.n_kblk);
   const int grp = id / (G * n_bg);
   const int in_grp = min(G, p.n_kblk - grp * G);
   const int rem = id - grp * G * n_bg;
